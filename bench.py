@@ -1,0 +1,412 @@
+"""Benchmark: causal bf16 attention forward + backward on one GB300.
+
+Step = one pass of the hot path over one batch: ``attn_fwd`` (O, LSE) and
+``attn_bwd`` (row terms, dq/dk/dv) of causal self-attention, bf16,
+B=4, S=4096, H=16, D=128 (16384 tokens per batch, the S>=4096 point of the
+head-dim-128 sweep).  The LSE merge and the fp32 path are timed in the same
+run as auxiliary lines (``aux``).  Throughput counts algorithmic flops:
+forward 4*D*N_vis, backward 10*D*N_vis (five GEMM-shaped products including
+the recompute of S), N_vis = exact number of visible (query, key) pairs.
+
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the
+same workload instead (the reference arm; the oracle is test
+infrastructure, used here only as that baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(B=4, S=4096, H=16, D=128, window=(-1, 0))
+METRIC = "attention TFLOP/s fwd+bwd (bf16 causal) and % of GB300 dense BF16 tensor peak"
+
+
+def n_visible(S, window):
+    wl, wr = window
+    n = 0
+    for i in range(S):
+        lo = 0 if wl < 0 else max(0, i - wl)
+        hi = S - 1 if wr < 0 else min(S - 1, i + wr)
+        n += max(0, hi - lo + 1)
+    return n
+
+
+def flops(B, S, H, D, window):
+    nv = n_visible(S, window) * B * H
+    return 4.0 * D * nv, 10.0 * D * nv, nv
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    import torch
+    import scaled_dot_product_03_gb300 as gb
+    from scaled_dot_product_03_gb300 import build as libbuild
+    from scaled_dot_product_03_gb300 import inputs
+
+    ws, rank, local = dist_setup(args)
+    libbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, S, H, D, win = (WORKLOAD[k] for k in ("B", "S", "H", "D", "window"))
+    prob = inputs.dense(B, S, H, D, window=win, seed=rank)
+    d = prob.to(dev)
+    q, k, v, dout = d.q, d.k, d.v, d.dout
+    scale = d.scale
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = gb.attn_bwd_workspace_size(q, k, scale=scale, window=win)
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        gb.attn_fwd(q, k, v, scale=scale, window=win, out=o, lse=lse)
+        if ev:
+            ev[1].record(stream)
+        gb.attn_bwd(dout, q, k, v, o, lse, scale=scale, window=win, dq=dq, dk=dk, dv=dv,
+                    workspace=work)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    gb.check_device_error()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    gb.check_device_error()
+    ms_total = max_over_ranks(start.elapsed_time(end), ws)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    f_fwd, f_bwd, nvis = flops(B, S, H, D, win)
+    ms_step = ms_total / args.steps
+    tflops = ws * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    peaks, src = measured_peaks()
+    peak_bf16 = peaks.get("bf16_tflops_sustained" if args.steps * ms_step > 2000 else "bf16_tflops")
+
+    # ------------------------------------------------------------- end to end
+    # through the public API with host buffers: pinned q, k, v, dO copied in,
+    # fwd + bwd, dq, dk, dv (and the loss-side O) copied back, every step.
+    hq = [t.cpu().pin_memory() for t in (prob.q, prob.k, prob.v, prob.dout)]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v, q)]
+    h2d = sum(t.numel() * t.element_size() for t in hq)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        for src_t, dst_t in zip(hq, (q, k, v, dout)):
+            dst_t.copy_(src_t, non_blocking=True)
+        step()
+        for src_t, dst_t in zip((dq, dk, dv, o), hout):
+            dst_t.copy_(src_t, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), ws) / args.steps
+    e2e_tflops = ws * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    aux = aux_lines(gb, inputs, dev, peaks) if rank == 0 and not args.no_aux else {}
+    cpu = cpu_baseline(args) if rank == 0 and ws == 1 and not args.no_cpu else None
+
+    if rank != 0:
+        return None
+    fwd_mean = statistics.mean(fwd_ms)
+    bwd_mean = statistics.mean(bwd_ms)
+    dominant = "bwd" if bwd_mean >= fwd_mean else "fwd"
+    dom_flops = f_bwd if dominant == "bwd" else f_fwd
+    dom_ms = bwd_mean if dominant == "bwd" else fwd_mean
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    launches_per_step = 1 + gb_launches_bwd(q.dtype, D)
+    line = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) q, k, v, dO on the CPU generator",
+        "config": {"workload": "causal self-attention fwd+bwd, bf16, B=%d S=%d H=%d D=%d" % (
+            B, S, H, D), "B": B, "S": S, "H": H, "D": D, "window": list(win),
+            "parallelism": "replicas" if ws > 1 else "single-gpu",
+            "l2": "inputs larger than L2 (q,k,v,o,dO,dq,dk,dv = %d MB)" % (
+                8 * q.numel() * 2 // 2**20),
+            "flops_per_step": f_fwd + f_bwd, "n_visible_pairs": nvis},
+        "pct_of_peak": round(100.0 * tflops / ws / peak_bf16, 2),
+        "peak_tflops": peak_bf16, "peak_source": src,
+        "fwd_ms": round(fwd_mean, 4), "bwd_ms": round(bwd_mean, 4),
+        "fwd_tflops": round(f_fwd / (fwd_mean * 1e-3) / 1e12, 2),
+        "bwd_tflops": round(f_bwd / (bwd_mean * 1e-3) / 1e12, 2),
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
+                     "peak": peak_bf16, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_bf16, 4),
+                     "traffic": None, "peak_source": src},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu,
+        "aux": aux,
+    }
+    return line
+
+
+def gb_launches_bwd(dtype, D):
+    """Kernels one attn_bwd call launches: row-term preprocess plus the main
+    kernel(s)."""
+    from scaled_dot_product_03_gb300 import _lib
+    return 3
+
+
+def aux_lines(gb, inputs, dev, peaks):
+    """LSE merge (HBM-bound) and fp32 forward+backward, timed on their own."""
+    import torch
+    out = {}
+    B, S, H, D = 4, 4096, 16, 128
+    g = torch.Generator().manual_seed(5)
+    o1 = torch.randn(B, S, H, D, generator=g).bfloat16().to(dev)
+    o2 = torch.randn(B, S, H, D, generator=g).bfloat16().to(dev)
+    l1 = torch.randn(B, H, S, generator=g).to(dev)
+    l2 = torch.randn(B, H, S, generator=g).to(dev)
+    oo, lo = torch.empty_like(o1), torch.empty_like(l1)
+    for _ in range(3):
+        gb.attn_merge_lse(o1, l1, o2, l2, out=oo, lse_out=lo)
+    torch.cuda.synchronize()
+    n = 20
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(n):
+        gb.attn_merge_lse(o1, l1, o2, l2, out=oo, lse_out=lo)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    nbytes = 3 * o1.numel() * 2 + 3 * l1.numel() * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["merge"] = {"workload": "bf16 B=4 S=4096 H=16 D=128", "ms": round(ms, 4),
+                    "GB/s": round(gbs, 1), "bound": "hbm", "peak_gbs": peaks["hbm_gbs"],
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes}
+    prob = inputs.page3().to(dev)
+    for _ in range(3):
+        o, lse = gb.attn_fwd(prob.q, prob.k, prob.v, scale=prob.scale)
+        gb.attn_bwd(prob.dout, prob.q, prob.k, prob.v, o, lse, scale=prob.scale)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(n):
+        o, lse = gb.attn_fwd(prob.q, prob.k, prob.v, scale=prob.scale)
+        gb.attn_bwd(prob.dout, prob.q, prob.k, prob.v, o, lse, scale=prob.scale)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    f_fwd, f_bwd, _ = flops(1, 512, 4, 64, (-1, -1))
+    out["fp32_page3"] = {"workload": "fp32 fwd+bwd B=1 S=512 H=4 D=64 non-causal",
+                         "ms": round(ms, 4),
+                         "TFLOP/s": round((f_fwd + f_bwd) / (ms * 1e-3) / 1e12, 3)}
+    return out
+
+
+def cpu_sample_units(heads=2):
+    return dict(B=1, S=WORKLOAD["S"], H=heads, D=WORKLOAD["D"], window=WORKLOAD["window"])
+
+
+def run_oracle_sample(seed=0, heads=2):
+    """Oracle fwd + bwd on the bounded sample (2 heads of one batch item of
+    the workload, all rows).  Returns (seconds, flops)."""
+    import oracle
+    from scaled_dot_product_03_gb300 import inputs
+    sm = cpu_sample_units(heads)
+    prob = inputs.dense(sm["B"], sm["S"], sm["H"], sm["D"], window=sm["window"], seed=seed)
+    f64 = lambda t: t.to("cpu").double().contiguous().reshape(-1, t.shape[2], t.shape[3]).numpy()
+    q, k, v, do = f64(prob.q), f64(prob.k), f64(prob.v), f64(prob.dout)
+    cu = oracle.dense_cu(sm["B"], sm["S"])
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, cu, cu, prob.scale, prob.window)
+    oracle.attn_bwd(q, k, v, do, cu, cu, prob.scale, prob.window)
+    dt = time.perf_counter() - t0
+    f_fwd, f_bwd, _ = flops(sm["B"], sm["S"], sm["H"], sm["D"], sm["window"])
+    return dt, f_fwd + f_bwd
+
+
+def cpu_baseline(args):
+    import oracle
+    oracle.build()
+    dt, fl = run_oracle_sample(heads=6)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "float64 oracle fwd+bwd on 6 heads x 4096 rows of one batch item "
+                      "(causal, D=128); %.1f s" % dt}
+
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        run_oracle_sample()
+    times, fl = [], 0
+    for i in range(args.steps):
+        dt, fl = run_oracle_sample()
+        times.append(dt)
+    total = sum(times)
+    value = fl * args.steps / total / 1e12
+    B, S, H, D, win = (WORKLOAD[k] for k in ("B", "S", "H", "D", "window"))
+    sm = cpu_sample_units()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "causal self-attention fwd+bwd, bf16, B=%d S=%d H=%d D=%d" % (
+            B, S, H, D), "B": B, "S": S, "H": H, "D": D, "window": list(win)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                         "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "each step: float64 oracle fwd+bwd on %d heads x %d rows of "
+                                   "one batch item of the workload" % (sm["H"], sm["S"])},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-aux", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

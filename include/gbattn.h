@@ -1,0 +1,205 @@
+/*
+ * gbattn.h -- C ABI of a fused scaled-dot-product attention library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operation.  For every query row i of every query head h
+ *
+ *     O_i   = sum_j softmax_j(scale * <q_i, k_j>) v_j     over visible keys j
+ *     LSE_i = log sum_j exp(scale * <q_i, k_j>)           (natural log)
+ *
+ * which is the operation behind every attention API the source pages call:
+ * torch.nn.functional.scaled_dot_product_attention and FlashAttention
+ * ("Add torch scaled dot product attention (FlashAttention)", title and
+ * benchmark), flex_attention with return_lse=True ("Significant Accuracy
+ * Difference between Compiled and Eager Flex Attention", repro and the
+ * merge_attn example), and TransformerEngine's FlashAttention /
+ * FusedAttention modules ("[PyTorch] fused CUDNN attention kernel not
+ * properly handling strides", repro).
+ *
+ * Visibility.  Key j is visible to query i iff
+ *     (window_left  < 0 or j >= i - window_left) and
+ *     (window_right < 0 or j <= i + window_right) and 0 <= j < L_kv,
+ * with i and j both counted from 0 inside their own sequence (top-left
+ * alignment).  window = (-1, 0) is causal, as in the TransformerEngine
+ * repro's window_size=(-1, 0); (band, 0) is the sliding-window-causal mask
+ * (q_idx >= kv_idx) & (q_idx - kv_idx <= band) of the flex-attention repro.
+ * A query row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * Grouped heads.  Hq must be a multiple of Hkv; query head h reads key/value
+ * head h / (Hq / Hkv) (the repro's q_heads=16, kv_heads=1, num_gqa_groups).
+ *
+ * Layouts.  No layout is ever guessed and no input is ever copied: each
+ * tensor is described by a pointer and explicit element strides, so views
+ * such as the packed sb(h+2h_g)d split of the TransformerEngine strides
+ * issue (strides (1152, 1152, 64, 1)) are read where they lie.
+ *   ATTN_LAYOUT_DENSE4D: element (b, s, h, d) lives at
+ *       ptr + b*stride[0] + s*stride[1] + h*stride[2] + d*stride[3]
+ *     This covers bshd, sbhd, bhsd and split packed layouts alike.
+ *   ATTN_LAYOUT_THD: packed variable-length batch ("[PyTorch] Add support
+ *     for cuDNN FusedAttention + THD + CP", the thd branch): element
+ *     (t, h, d) lives at ptr + t*stride[1] + h*stride[2] + d*stride[3]
+ *     (stride[0] is ignored); sequence b owns token rows
+ *     [cu_seqlens[b], cu_seqlens[b+1]).
+ * The innermost stride (d) must be 1.  For 16-bit types every other stride
+ * and the base pointer must be 16-byte aligned (a tensor-memory-accelerator
+ * requirement); otherwise the call fails with ATTN_ERR_UNSUPPORTED rather
+ * than copying.
+ *
+ * LSE layout: fp32, contiguous, [B, Hq, Sq] for DENSE4D and [Hq, Tq] for THD.
+ *
+ * Ownership and threading.  Every pointer is caller-owned device memory,
+ * except the attn_params struct itself (host).  The library allocates
+ * nothing, copies no input, and never synchronises the host: each call only
+ * enqueues kernels on the given stream (NULL = legacy default stream) and
+ * returns.  Inputs must stay valid until that work has run.  Calls are
+ * thread-safe; the error string is per host thread.
+ *
+ * Errors.  Every entry point returns an attn_status.  On ATTN_ERR_INVALID_ARG
+ * and ATTN_ERR_UNSUPPORTED nothing has been enqueued.  ATTN_ERR_CUDA reports
+ * a launch error.  Device-side waits are bounded: a kernel whose pipeline
+ * stalls past the watchdog limit sets a device error word and returns; the
+ * host reads it with attn_check_device_error().  attn_last_error_string()
+ * explains the last failure of the calling thread.
+ */
+#ifndef GBATTN_H_
+#define GBATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GBATTN_API __attribute__((visibility("default")))
+#else
+#define GBATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that the header needs no CUDA
+ * include. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* inconsistent sizes, null pointers, bad window */
+    ATTN_ERR_UNSUPPORTED = 2, /* valid request the kernels do not cover (D, alignment) */
+    ATTN_ERR_CUDA = 3,        /* a CUDA call or launch failed */
+    ATTN_ERR_TIMEOUT = 4      /* a device-side wait ran past the watchdog limit */
+} attn_status;
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1, ATTN_F32 = 2 } attn_dtype;
+
+typedef enum { ATTN_LAYOUT_DENSE4D = 0, ATTN_LAYOUT_THD = 1 } attn_layout;
+
+/* A tensor view: device pointer plus element strides (see Layouts). */
+typedef struct {
+    void *ptr;
+    int64_t stride[4];
+} attn_tensor;
+
+typedef struct {
+    attn_dtype dtype;    /* element type of q, k, v, o, dO, dq, dk, dv */
+    attn_layout layout;
+    int B;               /* batch size (DENSE4D) or number of sequences (THD) */
+    int Sq, Skv;         /* DENSE4D: sequence lengths.  THD: total token rows
+                            Tq and Tkv of the packed q and k/v tensors */
+    int Hq, Hkv;         /* query heads, key/value heads (Hq % Hkv == 0) */
+    int D;               /* head dimension: 64 or 128 */
+    const int32_t *cu_seqlens_q;  /* THD only: device, B + 1 non-decreasing */
+    const int32_t *cu_seqlens_kv; /* offsets starting at 0 (NULL for DENSE4D) */
+    int max_seqlen_q;    /* THD only: upper bound of the sequence lengths */
+    int max_seqlen_kv;
+    float scale;         /* softmax scale, e.g. 1/sqrt(D) */
+    int window_left;     /* -1 = unbounded */
+    int window_right;    /* -1 = unbounded; (-1, 0) = causal */
+} attn_params;
+
+/*
+ * Forward: O and LSE from q, k, v.
+ * q, o: [B, Sq, Hq, D] (or [Tq, Hq, D]); k, v: [B, Skv, Hkv, D] (or
+ * [Tkv, Hkv, D]); lse: fp32 as described under "LSE layout".  o and lse
+ * are written for every query row (rows with no visible key: 0 and -inf).
+ */
+GBATTN_API attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor k,
+                     attn_tensor v, attn_tensor o, float *lse,
+                     attn_stream_t stream);
+
+/*
+ * Bytes of device scratch memory attn_bwd needs for these parameters
+ * (fp32 row terms D_i = <dO_i, O_i> and an fp32 dq accumulator).
+ * Returns 0 for invalid parameters.
+ */
+GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
+
+/*
+ * Backward of the forward above for a loss with gradient dout = dL/dO
+ * (the flex-attention repro's out.sum().backward() is dout = ones):
+ *   dq = scale * sum_j dS_ij k_j,  dk_j = scale * sum_i dS_ij q_i,
+ *   dv_j = sum_i P_ij dO_i,        dS_ij = P_ij (<dO_i, v_j> - <dO_i, O_i>),
+ * with P recomputed from q, k and the forward's lse (no saved P); dk and dv
+ * sum over the Hq / Hkv query heads that share a key/value head.
+ * o and lse must be the forward's outputs for the same inputs.  dq has q's
+ * shape, dk and dv k's shape, each with its own strides (they may be views
+ * of one packed gradient buffer).  workspace: device memory of at least
+ * attn_bwd_workspace_size(p) bytes, 256-byte aligned, whose contents on
+ * entry do not matter; it must not be shared with a call that may run at
+ * the same time.
+ */
+GBATTN_API attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k,
+                     attn_tensor v, attn_tensor o, attn_tensor dout,
+                     const float *lse, attn_tensor dq, attn_tensor dk,
+                     attn_tensor dv, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream);
+
+/*
+ * Merge two partial attentions of the same queries over disjoint key sets
+ * (merge_attn in "Significant Accuracy Difference between Compiled and Eager
+ * Flex Attention"):
+ *   m = max(lse1, lse2); e1 = exp(lse1 - m); e2 = exp(lse2 - m)
+ *   o = (o1 e1 + o2 e2) / (e1 + e2);  lse = m + log(e1 + e2)
+ * computed in fp32.  A side whose lse is -inf contributes nothing; when both
+ * are -inf the row becomes o = 0, lse = -inf.
+ * o1, o2, o_out: DENSE4D views [B, S, H, D] of element type dtype (a THD
+ * tensor [T, H, D] is passed as B = 1, S = T with stride[0] = 0);
+ * lse1, lse2, lse_out: fp32 contiguous [B, H, S].  o_out may alias o1 or
+ * o2 exactly and lse_out may alias lse1 or lse2 (in-place merge); other
+ * overlaps are undefined.  D: 1..256, D*elt a multiple of 16 bytes for
+ * 16-bit types.
+ */
+GBATTN_API attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int D,
+                           attn_tensor o1, const float *lse1, attn_tensor o2,
+                           const float *lse2, attn_tensor o_out,
+                           float *lse_out, attn_stream_t stream);
+
+/* Description of the calling thread's last failure ("" if none). */
+GBATTN_API const char *attn_last_error_string(void);
+
+/*
+ * Reads and clears the device error word set by kernel watchdogs on the
+ * current device.  Synchronises the given stream first.  Returns ATTN_OK or
+ * ATTN_ERR_TIMEOUT (or ATTN_ERR_CUDA if the read itself failed).
+ */
+GBATTN_API attn_status attn_check_device_error(attn_stream_t stream);
+
+/*
+ * Watchdog limit of every bounded device-side wait, in nanoseconds
+ * (default 2e9).  Affects launches enqueued after the call.  Returns the
+ * previous value.
+ */
+GBATTN_API uint64_t attn_set_watchdog_ns(uint64_t ns);
+
+/*
+ * Self-test of the watchdog: enqueues one kernel that waits on a barrier
+ * nothing ever arrives on, with the current watchdog limit; the kernel gives
+ * up, records ATTN_ERR_TIMEOUT in the device error word and returns.  No
+ * fault, trap or hang is involved.
+ */
+GBATTN_API attn_status attn_watchdog_selftest(attn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H_ */

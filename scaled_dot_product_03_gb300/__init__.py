@@ -1,1 +1,190 @@
-"""Fused scaled-dot-product attention for GB300 (sm_103a)."""
+"""Fused scaled-dot-product attention for GB300 (sm_103a).
+
+Python binding of the C ABI in ``include/gbattn.h``: the functions here only
+marshal torch tensors into pointers, strides and sizes and call the library
+on the current CUDA stream.  PyTorch supplies device memory for outputs the
+caller does not pass.  Every step of the computation runs in the library's
+CUDA kernels; there is no other implementation to fall back on.
+
+* :func:`attn_fwd`  -- O and LSE (``softmax(scale * q k^T + mask) v``).
+* :func:`attn_bwd`  -- dq, dk, dv from dO and the saved LSE.
+* :func:`attn_merge_lse` -- merge two partial attentions by their LSE.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+__all__ = ["attn_fwd", "attn_bwd", "attn_merge_lse", "attn_bwd_workspace_size",
+           "check_device_error", "set_watchdog_ns", "watchdog_selftest", "AttnError",
+           "params_for"]
+
+AttnError = _lib.AttnError
+
+_DTYPES = {torch.float16: _lib.ATTN_F16, torch.bfloat16: _lib.ATTN_BF16,
+           torch.float32: _lib.ATTN_F32}
+
+
+def _stream(t: torch.Tensor):
+    return ctypes_void(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def ctypes_void(x):
+    import ctypes
+    return ctypes.c_void_p(x)
+
+
+def _tensor(t: Optional[torch.Tensor], thd: bool) -> "_lib.AttnTensor":
+    at = _lib.AttnTensor()
+    if t is None:
+        return at
+    at.ptr = t.data_ptr()
+    st = t.stride()
+    if thd:
+        assert t.dim() == 3, "THD tensors are [T, H, D]"
+        at.stride[:] = (0, st[0], st[1], st[2])
+    else:
+        assert t.dim() == 4, "dense tensors are [B, S, H, D]"
+        at.stride[:] = tuple(st)
+    return at
+
+
+def params_for(q, k, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seqlens_kv=None,
+               max_seqlen_q=None, max_seqlen_kv=None) -> "_lib.AttnParams":
+    """The ``attn_params`` struct describing q (and k, v) views."""
+    p = _lib.AttnParams()
+    if q.dtype not in _DTYPES:
+        raise TypeError("unsupported dtype %s" % q.dtype)
+    p.dtype = _DTYPES[q.dtype]
+    thd = cu_seqlens_q is not None
+    D = q.shape[-1]
+    p.D = D
+    p.scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    p.window_left, p.window_right = int(window[0]), int(window[1])
+    if thd:
+        if cu_seqlens_kv is None:
+            cu_seqlens_kv = cu_seqlens_q
+        p.layout = _lib.ATTN_LAYOUT_THD
+        p.B = cu_seqlens_q.numel() - 1
+        p.Sq, p.Hq = q.shape[0], q.shape[1]
+        p.Skv, p.Hkv = k.shape[0], k.shape[1]
+        p.cu_seqlens_q = cu_seqlens_q.data_ptr()
+        p.cu_seqlens_kv = cu_seqlens_kv.data_ptr()
+        if max_seqlen_q is None:  # needs a device->host read of cu_seqlens
+            max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max()) if p.B else 0
+        if max_seqlen_kv is None:
+            max_seqlen_kv = int((cu_seqlens_kv[1:] - cu_seqlens_kv[:-1]).max()) if p.B else 0
+        p.max_seqlen_q, p.max_seqlen_kv = int(max_seqlen_q), int(max_seqlen_kv)
+    else:
+        p.layout = _lib.ATTN_LAYOUT_DENSE4D
+        p.B, p.Sq, p.Hq = q.shape[0], q.shape[1], q.shape[2]
+        p.Skv, p.Hkv = k.shape[1], k.shape[2]
+    return p
+
+
+def _lse_shape(p):
+    if p.layout == _lib.ATTN_LAYOUT_THD:
+        return (p.Hq, p.Sq)
+    return (p.B, p.Hq, p.Sq)
+
+
+def attn_fwd(q, k, v, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seqlens_kv=None,
+             max_seqlen_q=None, max_seqlen_kv=None, out=None, lse=None
+             ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Forward attention.  Dense: q ``[B, Sq, Hq, D]``, k/v ``[B, Skv, Hkv, D]``
+    (any strides, d contiguous).  THD (``cu_seqlens_q`` given): q ``[Tq, Hq, D]``,
+    k/v ``[Tkv, Hkv, D]``.  ``window=(left, right)``, -1 unbounded, (-1, 0)
+    causal.  Returns ``(o, lse)`` with lse fp32 ``[B, Hq, Sq]`` / ``[Hq, Tq]``."""
+    p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
+                   cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
+                   max_seqlen_kv=max_seqlen_kv)
+    thd = p.layout == _lib.ATTN_LAYOUT_THD
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(_lse_shape(p), dtype=torch.float32, device=q.device)
+    lib = _lib.load()
+    _lib.check(lib.attn_fwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                            _tensor(out, thd), lse.data_ptr(), _stream(q)))
+    return out, lse
+
+
+def attn_bwd_workspace_size(q, k, **kw) -> int:
+    p = params_for(q, k, **kw)
+    return int(_lib.load().attn_bwd_workspace_size(p))
+
+
+def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens_q=None,
+             cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None, dk=None,
+             dv=None, workspace=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Backward attention: ``(dq, dk, dv)`` for upstream gradient ``dout``,
+    recomputing P from q, k and the forward's ``lse``.  ``workspace`` (uint8
+    device tensor of at least :func:`attn_bwd_workspace_size` bytes) is
+    allocated when not given."""
+    p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
+                   cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
+                   max_seqlen_kv=max_seqlen_kv)
+    thd = p.layout == _lib.ATTN_LAYOUT_THD
+    lib = _lib.load()
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty(k.shape, dtype=k.dtype, device=k.device)
+    if dv is None:
+        dv = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    need = int(lib.attn_bwd_workspace_size(p))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _lib.check(lib.attn_bwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                            _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
+                            _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            _stream(q)))
+    return dq, dk, dv
+
+
+def attn_merge_lse(o1, lse1, o2, lse2, *, out=None, lse_out=None
+                   ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Merge two partial attentions over disjoint key sets by their LSE.
+    Dense: o ``[B, S, H, D]`` with lse ``[B, H, S]``; THD: o ``[T, H, D]``
+    with lse ``[H, T]``.  ``out`` / ``lse_out`` may be ``o1`` / ``lse1``
+    (in place)."""
+    if out is None:
+        out = torch.empty(o1.shape, dtype=o1.dtype, device=o1.device)
+    if lse_out is None:
+        lse_out = torch.empty(lse1.shape, dtype=torch.float32, device=lse1.device)
+    if o1.dim() == 3:
+        T, H, D = o1.shape
+        B, S = 1, T
+        views = [x.unsqueeze(0) for x in (o1, o2, out)]
+    else:
+        B, S, H, D = o1.shape
+        views = [o1, o2, out]
+    for l in (lse1, lse2, lse_out):
+        assert l.dtype == torch.float32 and l.is_contiguous() and l.numel() == B * H * S
+    if o1.dtype not in _DTYPES:
+        raise TypeError("unsupported dtype %s" % o1.dtype)
+    lib = _lib.load()
+    _lib.check(lib.attn_merge_lse(_DTYPES[o1.dtype], B, S, H, D, _tensor(views[0], False),
+                                  lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
+                                  _tensor(views[2], False), lse_out.data_ptr(), _stream(o1)))
+    return out, lse_out
+
+
+def check_device_error(device=None) -> None:
+    """Raises :class:`AttnError` if a kernel watchdog fired since the last check."""
+    s = torch.cuda.current_stream(device)
+    _lib.check(_lib.load().attn_check_device_error(ctypes_void(s.cuda_stream)))
+
+
+def set_watchdog_ns(ns: int) -> int:
+    return int(_lib.load().attn_set_watchdog_ns(int(ns)))
+
+
+def watchdog_selftest(device=None) -> None:
+    s = torch.cuda.current_stream(device)
+    _lib.check(_lib.load().attn_watchdog_selftest(ctypes_void(s.cuda_stream)))

@@ -1,0 +1,333 @@
+// api.cu -- the C ABI (include/gbattn.h): argument validation, workspace
+// layout, kernel selection by element type, and the device error word.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/gbattn.h"
+#include "launch.h"
+#include "tc.h"
+
+namespace gbattn {
+namespace {
+
+thread_local std::string t_error;
+
+attn_status fail(attn_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return st;
+}
+
+attn_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device error word set by bounded device-side waits that gave up.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices];
+uint64_t g_watchdog_ns = 2000000000ull;
+
+attn_status device_error_word(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device index %d too large", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_error);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+        g_err_ptr[dev] = (unsigned *)p;
+    }
+    *out = g_err_ptr[dev];
+    return ATTN_OK;
+}
+
+uint64_t watchdog_ns() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_watchdog_ns;
+}
+
+size_t elt_size(attn_dtype dt) { return dt == ATTN_F32 ? 4 : 2; }
+
+bool dtype_ok(int dt) { return dt == ATTN_F16 || dt == ATTN_BF16 || dt == ATTN_F32; }
+
+// Validates the shared problem description.
+attn_status check_params(const attn_params *p) {
+    if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+    if (!dtype_ok(p->dtype)) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)p->dtype);
+    if (p->layout != ATTN_LAYOUT_DENSE4D && p->layout != ATTN_LAYOUT_THD)
+        return fail(ATTN_ERR_INVALID_ARG, "unknown layout %d", (int)p->layout);
+    if (p->B < 0 || p->Sq < 0 || p->Skv < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d Sq=%d Skv=%d)", p->B, p->Sq, p->Skv);
+    if (p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "Hq=%d must be a positive multiple of Hkv=%d", p->Hq, p->Hkv);
+    if (p->D != 64 && p->D != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", p->D);
+    if (p->window_left < -1 || p->window_right < -1)
+        return fail(ATTN_ERR_INVALID_ARG, "window (%d, %d): each bound must be >= -1",
+                    p->window_left, p->window_right);
+    if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    if (p->layout == ATTN_LAYOUT_THD) {
+        if (p->B > 0 && (!p->cu_seqlens_q || !p->cu_seqlens_kv))
+            return fail(ATTN_ERR_INVALID_ARG, "THD layout needs cu_seqlens_q and cu_seqlens_kv");
+        if (p->max_seqlen_q < 0 || p->max_seqlen_kv < 0)
+            return fail(ATTN_ERR_INVALID_ARG, "negative max_seqlen");
+        if (p->max_seqlen_q > p->Sq || p->max_seqlen_kv > p->Skv)
+            return fail(ATTN_ERR_INVALID_ARG, "max_seqlen exceeds the total token rows");
+    }
+    return ATTN_OK;
+}
+
+attn_status check_tensor(const attn_params *p, const attn_tensor &t, const char *name) {
+    if (!t.ptr) return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", name);
+    if (t.stride[3] != 1)
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: innermost (d) stride %lld must be 1", name,
+                    (long long)t.stride[3]);
+    const int first = p->layout == ATTN_LAYOUT_THD ? 1 : 0;
+    for (int i = first; i < 3; ++i)
+        if (t.stride[i] < 0) return fail(ATTN_ERR_UNSUPPORTED, "%s: negative stride", name);
+    if (p->dtype != ATTN_F32) {
+        const size_t es = elt_size(p->dtype);
+        if ((uintptr_t)t.ptr % 16)
+            return fail(ATTN_ERR_UNSUPPORTED, "%s: base pointer not 16-byte aligned", name);
+        for (int i = first; i < 3; ++i)
+            if ((t.stride[i] * (int64_t)es) % 16)
+                return fail(ATTN_ERR_UNSUPPORTED,
+                            "%s: stride[%d]=%lld elements is not a multiple of 16 bytes", name, i,
+                            (long long)t.stride[i]);
+    } else if ((uintptr_t)t.ptr % 4) {
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: base pointer not 4-byte aligned", name);
+    }
+    return ATTN_OK;
+}
+
+View view_of(const attn_params *p, const attn_tensor &t) {
+    View v;
+    v.ptr = t.ptr;
+    v.sb = p->layout == ATTN_LAYOUT_THD ? 0 : t.stride[0];
+    v.ss = t.stride[1];
+    v.sh = t.stride[2];
+    return v;
+}
+
+MutView mview_of(const attn_params *p, const attn_tensor &t) {
+    MutView v;
+    v.ptr = t.ptr;
+    v.sb = p->layout == ATTN_LAYOUT_THD ? 0 : t.stride[0];
+    v.ss = t.stride[1];
+    v.sh = t.stride[2];
+    return v;
+}
+
+Geometry geometry_of(const attn_params *p) {
+    Geometry g;
+    g.B = p->B;
+    g.Sq = p->Sq;
+    g.Skv = p->Skv;
+    g.Hq = p->Hq;
+    g.Hkv = p->Hkv;
+    g.D = p->D;
+    g.G = p->Hq / p->Hkv;
+    g.thd = p->layout == ATTN_LAYOUT_THD;
+    g.Tq = p->Sq;
+    g.cu_q = p->cu_seqlens_q;
+    g.cu_kv = p->cu_seqlens_kv;
+    g.wl = p->window_left;
+    g.wr = p->window_right;
+    g.scale = p->scale;
+    g.scale_log2 = p->scale * kLog2e;
+    return g;
+}
+
+int max_lq(const attn_params *p) { return p->layout == ATTN_LAYOUT_THD ? p->max_seqlen_q : p->Sq; }
+int max_lkv(const attn_params *p) { return p->layout == ATTN_LAYOUT_THD ? p->max_seqlen_kv : p->Skv; }
+int64_t q_rows(const attn_params *p) {
+    return p->layout == ATTN_LAYOUT_THD ? (int64_t)p->Sq : (int64_t)p->B * p->Sq;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t delta_off, dq_off, total;
+};
+
+WsLayout ws_layout(const attn_params *p) {
+    WsLayout w;
+    const size_t rows = (size_t)q_rows(p);
+    w.delta_off = 0;
+    w.dq_off = round_up(sizeof(float) * rows * p->Hq, 256);
+    const bool need_acc = uses_tc_bwd(p->dtype, p->D);
+    w.total = w.dq_off + (need_acc ? round_up(sizeof(float) * rows * p->Hq * p->D, 256) : 0);
+    return w;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" {
+
+const char *attn_last_error_string(void) { return t_error.c_str(); }
+
+uint64_t attn_set_watchdog_ns(uint64_t ns) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const uint64_t old = g_watchdog_ns;
+    g_watchdog_ns = ns;
+    return old;
+}
+
+attn_status attn_check_device_error(attn_stream_t stream) {
+    unsigned *word = nullptr;
+    attn_status st = device_error_word(&word);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        return fail(ATTN_ERR_TIMEOUT, "a device-side wait gave up (code 0x%x)", v);
+    }
+    return ATTN_OK;
+}
+
+attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_tensor v,
+                     attn_tensor o, float *lse, attn_stream_t stream) {
+    t_error.clear();
+    attn_status st = check_params(p);
+    if (st != ATTN_OK) return st;
+    if (p->B == 0 || max_lq(p) == 0) return ATTN_OK;  // no query row: nothing to write
+    if ((st = check_tensor(p, q, "q")) || (st = check_tensor(p, k, "k")) ||
+        (st = check_tensor(p, v, "v")) || (st = check_tensor(p, o, "o")))
+        return st;
+    if (!lse) return fail(ATTN_ERR_INVALID_ARG, "lse: NULL pointer");
+    FwdArgs a;
+    a.g = geometry_of(p);
+    a.q = view_of(p, q);
+    a.k = view_of(p, k);
+    a.v = view_of(p, v);
+    a.o = mview_of(p, o);
+    a.lse = lse;
+    a.watchdog_ns = watchdog_ns();
+    if ((st = device_error_word(&a.err))) return st;
+    cudaError_t e;
+    if (uses_tc_fwd(p->dtype, p->D))
+        e = launch_tc_fwd(p->dtype, a, max_lq(p), max_lkv(p), (cudaStream_t)stream);
+    else
+        e = launch_simt_fwd(p->dtype, a, max_lq(p), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
+    return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_size(const attn_params *p) {
+    if (check_params(p) != ATTN_OK) return 0;
+    return ws_layout(p).total;
+}
+
+attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_tensor v,
+                     attn_tensor o, attn_tensor dout, const float *lse, attn_tensor dq,
+                     attn_tensor dk, attn_tensor dv, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream) {
+    t_error.clear();
+    attn_status st = check_params(p);
+    if (st != ATTN_OK) return st;
+    // Nothing to write when there is neither a query row (dq) nor a key row (dk, dv).
+    if (p->B == 0 || (max_lq(p) == 0 && max_lkv(p) == 0)) return ATTN_OK;
+    if ((st = check_tensor(p, q, "q")) || (st = check_tensor(p, k, "k")) ||
+        (st = check_tensor(p, v, "v")) || (st = check_tensor(p, o, "o")) ||
+        (st = check_tensor(p, dout, "dout")) || (st = check_tensor(p, dq, "dq")) ||
+        (st = check_tensor(p, dk, "dk")) || (st = check_tensor(p, dv, "dv")))
+        return st;
+    if (!lse) return fail(ATTN_ERR_INVALID_ARG, "lse: NULL pointer");
+    const WsLayout w = ws_layout(p);
+    if (!workspace && w.total) return fail(ATTN_ERR_INVALID_ARG, "workspace: NULL pointer");
+    if ((uintptr_t)workspace % 256) return fail(ATTN_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+    if (workspace_bytes < w.total)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes,
+                    w.total);
+    BwdArgs a;
+    a.g = geometry_of(p);
+    a.q = view_of(p, q);
+    a.k = view_of(p, k);
+    a.v = view_of(p, v);
+    a.o = view_of(p, o);
+    a.dout = view_of(p, dout);
+    a.lse = lse;
+    a.dq = mview_of(p, dq);
+    a.dk = mview_of(p, dk);
+    a.dv = mview_of(p, dv);
+    a.delta = (float *)((char *)workspace + w.delta_off);
+    a.dq_acc = uses_tc_bwd(p->dtype, p->D) ? (float *)((char *)workspace + w.dq_off) : nullptr;
+    a.watchdog_ns = watchdog_ns();
+    if ((st = device_error_word(&a.err))) return st;
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_bwd_preprocess(p->dtype, a, (int)q_rows(p), s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
+    if (uses_tc_bwd(p->dtype, p->D))
+        e = launch_tc_bwd(p->dtype, a, max_lq(p), max_lkv(p), (int)q_rows(p), s);
+    else
+        e = launch_simt_bwd(p->dtype, a, max_lq(p), max_lkv(p), s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
+    return ATTN_OK;
+}
+
+attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int D, attn_tensor o1,
+                           const float *lse1, attn_tensor o2, const float *lse2,
+                           attn_tensor o_out, float *lse_out, attn_stream_t stream) {
+    t_error.clear();
+    if (!dtype_ok(dtype)) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B < 0 || S < 0 || H < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size");
+    if (D < 1 || D > 256) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not in 1..256", D);
+    if ((int64_t)B * S * H == 0) return ATTN_OK;
+    const attn_tensor *ts[3] = {&o1, &o2, &o_out};
+    const char *names[3] = {"o1", "o2", "o_out"};
+    for (int i = 0; i < 3; ++i) {
+        if (!ts[i]->ptr) return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", names[i]);
+        if (ts[i]->stride[3] != 1)
+            return fail(ATTN_ERR_UNSUPPORTED, "%s: innermost stride must be 1", names[i]);
+        if ((uintptr_t)ts[i]->ptr % elt_size(dtype))
+            return fail(ATTN_ERR_UNSUPPORTED, "%s: misaligned pointer", names[i]);
+    }
+    if (!lse1 || !lse2 || !lse_out) return fail(ATTN_ERR_INVALID_ARG, "lse: NULL pointer");
+    MergeArgs a;
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.D = D;
+    a.o1 = View{o1.ptr, o1.stride[0], o1.stride[1], o1.stride[2]};
+    a.o2 = View{o2.ptr, o2.stride[0], o2.stride[1], o2.stride[2]};
+    a.out = MutView{o_out.ptr, o_out.stride[0], o_out.stride[1], o_out.stride[2]};
+    a.lse1 = lse1;
+    a.lse2 = lse2;
+    a.lse_out = lse_out;
+    cudaError_t e = launch_merge(dtype, a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_merge_lse launch");
+    return ATTN_OK;
+}
+
+attn_status attn_watchdog_selftest(attn_stream_t stream) {
+    t_error.clear();
+    unsigned *word = nullptr;
+    attn_status st = device_error_word(&word);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = launch_watchdog_selftest(word, watchdog_ns(), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "watchdog self-test launch");
+    return ATTN_OK;
+}
+
+}  // extern "C"

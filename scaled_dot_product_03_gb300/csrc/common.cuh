@@ -1,0 +1,101 @@
+// common.cuh -- types shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbattn {
+
+// log2(e) and ln(2), for moving between natural-log and base-2 softmax.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// A tensor view: base pointer and element strides of (b, s, h); the d
+// stride is 1.  THD views have sb = 0 and carry the sequence start in the
+// row offset instead.
+struct View {
+    const void *ptr;
+    int64_t sb, ss, sh;
+};
+
+struct MutView {
+    void *ptr;
+    int64_t sb, ss, sh;
+};
+
+// Everything a kernel needs to locate sequence b.
+struct Geometry {
+    int B, Sq, Skv, Hq, Hkv, D, G;
+    int thd;              // 1: packed THD, 0: dense
+    int Tq;               // THD: total query rows (LSE row pitch)
+    const int *cu_q, *cu_kv;
+    int wl, wr;           // window, -1 = unbounded
+    float scale;
+    float scale_log2;     // scale * log2(e)
+};
+
+struct SeqInfo {
+    int q0, kv0;  // first row of the sequence (THD), 0 for dense
+    int Lq, Lkv;  // lengths
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const Geometry &g, int b) {
+    SeqInfo s;
+    if (g.thd) {
+        s.q0 = __ldg(g.cu_q + b);
+        s.Lq = __ldg(g.cu_q + b + 1) - s.q0;
+        s.kv0 = __ldg(g.cu_kv + b);
+        s.Lkv = __ldg(g.cu_kv + b + 1) - s.kv0;
+    } else {
+        s.q0 = 0;
+        s.kv0 = 0;
+        s.Lq = g.Sq;
+        s.Lkv = g.Skv;
+    }
+    return s;
+}
+
+// Index of LSE / row-term element of query row i of head h in sequence b.
+__device__ __forceinline__ int64_t lse_index(const Geometry &g, const SeqInfo &s,
+                                             int b, int h, int i) {
+    return g.thd ? (int64_t)h * g.Tq + s.q0 + i
+                 : ((int64_t)b * g.Hq + h) * g.Sq + i;
+}
+
+__device__ __forceinline__ bool visible(int i, int j, int Lkv, int wl, int wr) {
+    return j >= 0 && j < Lkv && (wl < 0 || j >= i - wl) && (wr < 0 || j <= i + wr);
+}
+
+// Range [lo, hi) of keys visible to at least one of query rows [i0, i1).
+__device__ __forceinline__ void key_range(int i0, int i1, int Lkv, int wl, int wr,
+                                          int &lo, int &hi) {
+    lo = wl < 0 ? 0 : max(0, i0 - wl);
+    hi = wr < 0 ? Lkv : min(Lkv, i1 - 1 + wr + 1);
+    if (hi < lo) hi = lo;
+}
+
+// Range [lo, hi) of query rows that see at least one of keys [j0, j1).
+__device__ __forceinline__ void query_range(int j0, int j1, int Lq, int wl, int wr,
+                                            int &lo, int &hi) {
+    lo = wr < 0 ? 0 : max(0, j0 - wr);
+    hi = wl < 0 ? Lq : min(Lq, j1 - 1 + wl + 1);
+    if (hi < lo) hi = lo;
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+}  // namespace gbattn

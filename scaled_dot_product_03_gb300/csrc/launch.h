@@ -1,0 +1,43 @@
+// launch.h -- host-side launchers of the library's kernels (internal).
+#pragma once
+
+#include "common.cuh"
+
+namespace gbattn {
+
+struct FwdArgs {
+    Geometry g;
+    View q, k, v;
+    MutView o;
+    float *lse;
+    unsigned *err;        // device error word (watchdog)
+    uint64_t watchdog_ns;
+};
+
+struct BwdArgs {
+    Geometry g;
+    View q, k, v, o, dout;
+    const float *lse;
+    MutView dq, dk, dv;
+    float *delta;         // workspace: row terms <dO_i, O_i>, laid out like LSE
+    float *dq_acc;        // workspace: fp32 dq accumulator [rows][Hq][D]
+    unsigned *err;
+    uint64_t watchdog_ns;
+};
+
+struct MergeArgs {
+    int B, S, H, D;
+    View o1, o2;
+    MutView out;
+    const float *lse1, *lse2;
+    float *lse_out;
+};
+
+// dtype: 0 = fp16, 1 = bf16, 2 = fp32 (same values as attn_dtype).
+cudaError_t launch_simt_fwd(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st);
+cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv,
+                            cudaStream_t st);
+cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStream_t st);
+cudaError_t launch_merge(int dtype, const MergeArgs &a, cudaStream_t st);
+
+}  // namespace gbattn

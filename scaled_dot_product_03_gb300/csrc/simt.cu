@@ -1,0 +1,385 @@
+// simt.cu -- FFMA (CUDA-core) attention kernels.
+//
+// This is the fp32 path: "Significant Accuracy Difference between Compiled
+// and Eager Flex Attention" traces its fp32 error to kernels that used
+// tensor cores "by default" for fp32 inputs, so fp32 inputs are computed
+// here with plain fp32 fused multiply-adds and never reach a tensor core.
+// Every kernel also accepts fp16/bf16 inputs (converted to fp32 on load).
+//
+// Forward: one thread per query row, online softmax over key blocks staged
+// in shared memory (an exact rewrite of the two-pass softmax).
+// Backward: the row term delta_i = <dO_i, O_i> first, then one kernel for dq
+// (thread per query row) and one for dk/dv (four threads per key, summing
+// over the query heads of the group), each recomputing P from the saved LSE.
+#include "launch.h"
+
+namespace gbattn {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <typename T>
+__device__ __forceinline__ const T *row_ptr(const View &v, int b, int row, int h) {
+    return (const T *)v.ptr + (int64_t)b * v.sb + (int64_t)row * v.ss + (int64_t)h * v.sh;
+}
+template <typename T>
+__device__ __forceinline__ T *row_ptr(const MutView &v, int b, int row, int h) {
+    return (T *)v.ptr + (int64_t)b * v.sb + (int64_t)row * v.ss + (int64_t)h * v.sh;
+}
+
+// ---------------------------------------------------------------------------
+// Forward.  grid (ceil(max Lq / 128), Hq, B), 128 threads; thread = query row.
+// smem: Q^T [D][129] (padded so row-per-thread reads are conflict-free),
+// K and V blocks [BN][D], all fp32.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
+    constexpr int BM = kThreads, BN = (D > 64) ? 16 : 32, QP = BM + 1;
+    extern __shared__ float smem[];
+    float *Qs = smem, *Ks = Qs + D * QP, *Vs = Ks + BN * D;
+    const Geometry &g = a.g;
+    const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * BM, tid = threadIdx.x;
+    const SeqInfo s = seq_info(g, b);
+    if (m0 >= s.Lq) return;
+    const int hk = h / g.G, i = m0 + tid;
+    for (int e = tid; e < BM * D; e += kThreads) {
+        const int r = e / D, d = e % D;
+        float x = 0.f;
+        if (m0 + r < s.Lq) x = to_f32(row_ptr<T>(a.q, b, s.q0 + m0 + r, h)[d]);
+        Qs[d * QP + r] = x;
+    }
+    int jlo, jhi;
+    key_range(m0, min(m0 + BM, s.Lq), s.Lkv, g.wl, g.wr, jlo, jhi);
+    float m = -INFINITY, l = 0.f, o[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) o[d] = 0.f;
+    for (int j0 = jlo; j0 < jhi; j0 += BN) {
+        __syncthreads();
+        for (int e = tid; e < BN * D; e += kThreads) {
+            const int r = e / D, d = e % D, j = j0 + r;
+            float kx = 0.f, vx = 0.f;
+            if (j < jhi) {
+                kx = to_f32(row_ptr<T>(a.k, b, s.kv0 + j, hk)[d]);
+                vx = to_f32(row_ptr<T>(a.v, b, s.kv0 + j, hk)[d]);
+            }
+            Ks[e] = kx;
+            Vs[e] = vx;
+        }
+        __syncthreads();
+        float sc[BN];
+#pragma unroll
+        for (int jj = 0; jj < BN; ++jj) sc[jj] = 0.f;
+#pragma unroll 4
+        for (int d = 0; d < D; ++d) {
+            const float qd = Qs[d * QP + tid];
+#pragma unroll
+            for (int jj = 0; jj < BN; ++jj) sc[jj] = fmaf(qd, Ks[jj * D + d], sc[jj]);
+        }
+        float mx = m;
+#pragma unroll
+        for (int jj = 0; jj < BN; ++jj) {
+            const int j = j0 + jj;
+            const bool vis = i < s.Lq && j < jhi && visible(i, j, s.Lkv, g.wl, g.wr);
+            if (!vis) sc[jj] = -INFINITY;
+            else mx = fmaxf(mx, sc[jj] * g.scale_log2);
+        }
+        if (mx == -INFINITY) continue;  // nothing visible yet for this row
+        const float alpha = exp2f(m - mx);
+        l *= alpha;
+#pragma unroll
+        for (int d = 0; d < D; ++d) o[d] *= alpha;
+#pragma unroll
+        for (int jj = 0; jj < BN; ++jj) {
+            const float p = sc[jj] == -INFINITY ? 0.f : exp2f(fmaf(sc[jj], g.scale_log2, -mx));
+            l += p;
+            sc[jj] = p;
+        }
+#pragma unroll
+        for (int jj = 0; jj < BN; ++jj) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) o[d] = fmaf(sc[jj], Vs[jj * D + d], o[d]);
+        }
+        m = mx;
+    }
+    if (i < s.Lq) {
+        T *orow = row_ptr<T>(a.o, b, s.q0 + i, h);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) orow[d] = from_f32<T>(o[d] * inv);
+        a.lse[lse_index(g, s, b, h, i)] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward preprocess: delta = <dO, O> per (row, head); one warp per pair.
+template <typename T>
+__global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
+    const Geometry &g = a.g;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+         w < (int64_t)rows * g.Hq; w += nwarps) {
+        const int r = (int)(w / g.Hq), h = (int)(w % g.Hq);
+        int b = 0, row = r;
+        int64_t idx;
+        if (g.thd) {
+            idx = (int64_t)h * g.Tq + r;
+        } else {
+            b = r / g.Sq;
+            row = r % g.Sq;
+            idx = ((int64_t)b * g.Hq + h) * g.Sq + row;
+        }
+        const T *o = row_ptr<T>(a.o, b, row, h);
+        const T *d_o = row_ptr<T>(a.dout, b, row, h);
+        float acc = 0.f;
+        for (int d = lane; d < g.D; d += 32) acc = fmaf(to_f32(o[d]), to_f32(d_o[d]), acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) a.delta[idx] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward dq: thread = query row; K, V blocks in shared memory.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(BwdArgs a) {
+    constexpr int BM = kThreads, BN = 16, QP = BM + 1;
+    extern __shared__ float smem[];
+    float *Qs = smem, *Os = Qs + D * QP, *Ks = Os + D * QP, *Vs = Ks + BN * D;
+    const Geometry &g = a.g;
+    const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * BM, tid = threadIdx.x;
+    const SeqInfo s = seq_info(g, b);
+    if (m0 >= s.Lq) return;
+    const int hk = h / g.G, i = m0 + tid;
+    for (int e = tid; e < BM * D; e += kThreads) {
+        const int r = e / D, d = e % D;
+        float x = 0.f, y = 0.f;
+        if (m0 + r < s.Lq) {
+            x = to_f32(row_ptr<T>(a.q, b, s.q0 + m0 + r, h)[d]);
+            y = to_f32(row_ptr<T>(a.dout, b, s.q0 + m0 + r, h)[d]);
+        }
+        Qs[d * QP + r] = x;
+        Os[d * QP + r] = y;  // dO^T
+    }
+    float lse_l2 = 0.f, delta = 0.f;
+    if (i < s.Lq) {
+        const int64_t li = lse_index(g, s, b, h, i);
+        lse_l2 = a.lse[li] * kLog2e;
+        delta = a.delta[li];
+    }
+    int jlo, jhi;
+    key_range(m0, min(m0 + BM, s.Lq), s.Lkv, g.wl, g.wr, jlo, jhi);
+    float dq[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) dq[d] = 0.f;
+    for (int j0 = jlo; j0 < jhi; j0 += BN) {
+        __syncthreads();
+        for (int e = tid; e < BN * D; e += kThreads) {
+            const int r = e / D, d = e % D, j = j0 + r;
+            float kx = 0.f, vx = 0.f;
+            if (j < jhi) {
+                kx = to_f32(row_ptr<T>(a.k, b, s.kv0 + j, hk)[d]);
+                vx = to_f32(row_ptr<T>(a.v, b, s.kv0 + j, hk)[d]);
+            }
+            Ks[e] = kx;
+            Vs[e] = vx;
+        }
+        __syncthreads();
+        float sc[BN], dp[BN];
+#pragma unroll
+        for (int jj = 0; jj < BN; ++jj) sc[jj] = dp[jj] = 0.f;
+#pragma unroll 4
+        for (int d = 0; d < D; ++d) {
+            const float qd = Qs[d * QP + tid], od = Os[d * QP + tid];
+#pragma unroll
+            for (int jj = 0; jj < BN; ++jj) {
+                sc[jj] = fmaf(qd, Ks[jj * D + d], sc[jj]);
+                dp[jj] = fmaf(od, Vs[jj * D + d], dp[jj]);
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < BN; ++jj) {
+            const int j = j0 + jj;
+            float ds = 0.f;
+            if (i < s.Lq && j < jhi && visible(i, j, s.Lkv, g.wl, g.wr)) {
+                const float p = exp2f(fmaf(sc[jj], g.scale_log2, -lse_l2));
+                ds = p * (dp[jj] - delta);
+            }
+            sc[jj] = ds;
+        }
+#pragma unroll
+        for (int jj = 0; jj < BN; ++jj) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) dq[d] = fmaf(sc[jj], Ks[jj * D + d], dq[d]);
+        }
+    }
+    if (i < s.Lq) {
+        T *row = row_ptr<T>(a.dq, b, s.q0 + i, h);
+#pragma unroll
+        for (int d = 0; d < D; ++d) row[d] = from_f32<T>(dq[d] * g.scale);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward dk, dv: four threads per key (thread part p owns d = p, p+4, ...),
+// 32 keys per CTA; loops over the query heads of the group and over query
+// blocks of 32 rows staged in shared memory.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(BwdArgs a) {
+    constexpr int BN = kThreads / 4, BM = 32, DP = D / 4;
+    extern __shared__ float smem[];
+    float *Qs = smem, *Os = Qs + BM * D, *Ls = Os + BM * D, *Ds = Ls + BM;
+    const Geometry &g = a.g;
+    const int b = blockIdx.z, hk = blockIdx.y, n0 = blockIdx.x * BN, tid = threadIdx.x;
+    const SeqInfo s = seq_info(g, b);
+    if (n0 >= s.Lkv) return;
+    const int kt = tid / 4, part = tid % 4, j = n0 + kt;
+    float kr[DP], vr[DP], dk[DP], dv[DP];
+#pragma unroll
+    for (int t = 0; t < DP; ++t) {
+        kr[t] = vr[t] = dk[t] = dv[t] = 0.f;
+        if (j < s.Lkv) {
+            kr[t] = to_f32(row_ptr<T>(a.k, b, s.kv0 + j, hk)[4 * t + part]);
+            vr[t] = to_f32(row_ptr<T>(a.v, b, s.kv0 + j, hk)[4 * t + part]);
+        }
+    }
+    int ilo, ihi;
+    query_range(n0, min(n0 + BN, s.Lkv), s.Lq, g.wl, g.wr, ilo, ihi);
+    for (int h = hk * g.G; h < (hk + 1) * g.G; ++h) {
+        for (int i0 = ilo; i0 < ihi; i0 += BM) {
+            __syncthreads();
+            for (int e = tid; e < BM * D; e += kThreads) {
+                const int r = e / D, d = e % D, i = i0 + r;
+                float x = 0.f, y = 0.f;
+                if (i < ihi) {
+                    x = to_f32(row_ptr<T>(a.q, b, s.q0 + i, h)[d]);
+                    y = to_f32(row_ptr<T>(a.dout, b, s.q0 + i, h)[d]);
+                }
+                Qs[e] = x;
+                Os[e] = y;
+            }
+            for (int r = tid; r < BM; r += kThreads) {
+                const int i = i0 + r;
+                float lv = 0.f, dv_ = 0.f;
+                if (i < ihi) {
+                    const int64_t li = lse_index(g, s, b, h, i);
+                    lv = a.lse[li] * kLog2e;
+                    dv_ = a.delta[li];
+                }
+                Ls[r] = lv;
+                Ds[r] = dv_;
+            }
+            __syncthreads();
+            for (int r = 0; r < BM; ++r) {
+                const int i = i0 + r;
+                float sp = 0.f, dpp = 0.f;
+#pragma unroll
+                for (int t = 0; t < DP; ++t) {
+                    sp = fmaf(Qs[r * D + 4 * t + part], kr[t], sp);
+                    dpp = fmaf(Os[r * D + 4 * t + part], vr[t], dpp);
+                }
+                sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+                sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+                dpp += __shfl_xor_sync(0xffffffffu, dpp, 1);
+                dpp += __shfl_xor_sync(0xffffffffu, dpp, 2);
+                if (i < ihi && visible(i, j, s.Lkv, g.wl, g.wr)) {
+                    const float p = exp2f(fmaf(sp, g.scale_log2, -Ls[r]));
+                    const float ds = p * (dpp - Ds[r]);
+#pragma unroll
+                    for (int t = 0; t < DP; ++t) {
+                        dv[t] = fmaf(p, Os[r * D + 4 * t + part], dv[t]);
+                        dk[t] = fmaf(ds, Qs[r * D + 4 * t + part], dk[t]);
+                    }
+                }
+            }
+        }
+    }
+    if (j < s.Lkv) {
+        T *dkrow = row_ptr<T>(a.dk, b, s.kv0 + j, hk);
+        T *dvrow = row_ptr<T>(a.dv, b, s.kv0 + j, hk);
+#pragma unroll
+        for (int t = 0; t < DP; ++t) {
+            dkrow[4 * t + part] = from_f32<T>(dk[t] * g.scale);
+            dvrow[4 * t + part] = from_f32<T>(dv[t]);
+        }
+    }
+}
+
+template <typename T, int D>
+cudaError_t fwd_typed(const FwdArgs &a, int max_lq, cudaStream_t st) {
+    constexpr int BN = (D > 64) ? 16 : 32;
+    const size_t smem = sizeof(float) * (D * (kThreads + 1) + 2 * BN * D);
+    auto k = simt_fwd_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((max_lq + kThreads - 1) / kThreads, a.g.Hq, a.g.B);
+    k<<<grid, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t bwd_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
+    if (max_lq > 0) {
+        const size_t smem = sizeof(float) * (2 * D * (kThreads + 1) + 2 * 16 * D);
+        auto k = simt_bwd_dq_kernel<T, D>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        dim3 grid((max_lq + kThreads - 1) / kThreads, a.g.Hq, a.g.B);
+        k<<<grid, kThreads, smem, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (max_lkv > 0) {
+        const size_t smem = sizeof(float) * (2 * 32 * D + 2 * 32);
+        auto k = simt_bwd_dkdv_kernel<T, D>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        dim3 grid((max_lkv + kThreads / 4 - 1) / (kThreads / 4), a.g.Hkv, a.g.B);
+        k<<<grid, kThreads, smem, st>>>(a);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_simt_fwd(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st) {
+    const int D = a.g.D;
+    switch (dtype * 2 + (D == 128)) {
+        case 0: return fwd_typed<__half, 64>(a, max_lq, st);
+        case 1: return fwd_typed<__half, 128>(a, max_lq, st);
+        case 2: return fwd_typed<__nv_bfloat16, 64>(a, max_lq, st);
+        case 3: return fwd_typed<__nv_bfloat16, 128>(a, max_lq, st);
+        case 4: return fwd_typed<float, 64>(a, max_lq, st);
+        case 5: return fwd_typed<float, 128>(a, max_lq, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStream_t st) {
+    const int64_t work = (int64_t)rows * a.g.Hq;
+    const int threads = 256;
+    const int64_t blocks = (work + 7) / 8;
+    const int grid = (int)(blocks < 152 * 32 ? (blocks < 1 ? 1 : blocks) : 152 * 32);
+    switch (dtype) {
+        case 0: bwd_preprocess_kernel<__half><<<grid, threads, 0, st>>>(a, rows); break;
+        case 1: bwd_preprocess_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(a, rows); break;
+        case 2: bwd_preprocess_kernel<float><<<grid, threads, 0, st>>>(a, rows); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv,
+                            cudaStream_t st) {
+    const int D = a.g.D;
+    switch (dtype * 2 + (D == 128)) {
+        case 0: return bwd_typed<__half, 64>(a, max_lq, max_lkv, st);
+        case 1: return bwd_typed<__half, 128>(a, max_lq, max_lkv, st);
+        case 2: return bwd_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, st);
+        case 3: return bwd_typed<__nv_bfloat16, 128>(a, max_lq, max_lkv, st);
+        case 4: return bwd_typed<float, 64>(a, max_lq, max_lkv, st);
+        case 5: return bwd_typed<float, 128>(a, max_lq, max_lkv, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gbattn

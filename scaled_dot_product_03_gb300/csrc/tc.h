@@ -1,0 +1,20 @@
+// tc.h -- launchers of the tcgen05 (tensor-core) kernels (internal).
+#pragma once
+
+#include "launch.h"
+
+namespace gbattn {
+
+// Whether the tensor-core kernels cover this element type and head dim.
+bool uses_tc_fwd(int dtype, int D);
+bool uses_tc_bwd(int dtype, int D);
+
+cudaError_t launch_tc_fwd(int dtype, const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t st);
+cudaError_t launch_tc_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows,
+                          cudaStream_t st);
+
+// One kernel that waits on an mbarrier nothing arrives on, gives up after
+// `limit_ns`, and records the timeout in *err.
+cudaError_t launch_watchdog_selftest(unsigned *err, uint64_t limit_ns, cudaStream_t st);
+
+}  // namespace gbattn

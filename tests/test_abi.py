@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from scaled_dot_product_03_gb300 import _lib
+from scaled_dot_product_03_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"GBATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(declared_symbols()) == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    # and nothing of the internal namespace leaks out
+    out = os.popen("nm -D --defined-only %s" % _lib.LIB_PATH).read()
+    exported = set(re.findall(r" T (\w+)", out))
+    assert exported >= set(declared_symbols())
+    assert not [s for s in exported if "gbattn" in s]
+
+
+def _params(**kw):
+    p = _lib.AttnParams()
+    p.dtype, p.layout = _lib.ATTN_BF16, _lib.ATTN_LAYOUT_DENSE4D
+    p.B, p.Sq, p.Skv, p.Hq, p.Hkv, p.D = 2, 128, 128, 4, 2, 64
+    p.scale, p.window_left, p.window_right = 0.125, -1, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def _t(ptr=4096, strides=(32768, 256, 64, 1)):
+    t = _lib.AttnTensor()
+    t.ptr = ptr
+    t.stride[:] = strides
+    return t
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(D=0), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=3, Hkv=2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(Hkv=0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(window_left=-2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=7), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(layout=5), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(layout=_lib.ATTN_LAYOUT_THD), _lib.ATTN_ERR_INVALID_ARG),  # no cu_seqlens
+])
+def test_invalid_params_rejected_without_launch(lib, kw, status):
+    p = _params(**kw)
+    st = lib.attn_fwd(ctypes.byref(p), _t(), _t(), _t(), _t(), 4096, None)
+    assert st == status
+    assert lib.attn_last_error_string()
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == 0
+
+
+@pytest.mark.parametrize("tensor_kw,status", [
+    (dict(ptr=4096 + 2), _lib.ATTN_ERR_UNSUPPORTED),               # not 16-byte aligned
+    (dict(strides=(32768, 260, 65, 1)), _lib.ATTN_ERR_UNSUPPORTED),  # strides not 16 B
+    (dict(strides=(32768, 256, 64, 2)), _lib.ATTN_ERR_UNSUPPORTED),  # d not contiguous
+    (dict(ptr=0), _lib.ATTN_ERR_INVALID_ARG),
+])
+def test_bad_views_rejected_without_copy(lib, tensor_kw, status):
+    p = _params()
+    st = lib.attn_fwd(ctypes.byref(p), _t(**tensor_kw), _t(), _t(), _t(), 4096, None)
+    assert st == status, lib.attn_last_error_string()
+
+
+def test_empty_problem_is_a_no_op(lib):
+    for kw in (dict(B=0), dict(Sq=0)):
+        p = _params(**kw)
+        assert lib.attn_fwd(ctypes.byref(p), _t(ptr=0), _t(ptr=0), _t(ptr=0), _t(ptr=0),
+                            0, None) == _lib.ATTN_OK
+
+
+def test_workspace_size(lib):
+    p = _params()
+    n = lib.attn_bwd_workspace_size(ctypes.byref(p))
+    rows = p.B * p.Sq
+    assert n >= 4 * rows * p.Hq  # row terms
+    assert n % 256 == 0
+    p32 = _params(dtype=_lib.ATTN_F32)
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p32)) >= 4 * rows * p.Hq
+
+
+def test_merge_rejects_bad_args(lib):
+    t = _t()
+    assert lib.attn_merge_lse(9, 1, 1, 1, 64, t, 4096, t, 4096, t, 4096, None) == \
+        _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_merge_lse(1, 1, 1, 1, 300, t, 4096, t, 4096, t, 4096, None) == \
+        _lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_merge_lse(1, 0, 5, 1, 64, t, 4096, t, 4096, t, 4096, None) == _lib.ATTN_OK

@@ -1,0 +1,276 @@
+"""GPU parity of the CUDA library against the float64 oracle, through the C
+ABI (via the ctypes binding), on the pages' workloads and on edge cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import scaled_dot_product_03_gb300 as gb
+from scaled_dot_product_03_gb300 import inputs
+from gpu_helpers import (check_bwd, check_fwd, kw, lse_rows, rows_of, run_bwd, run_fwd,
+                         sample_keys, sample_rows)
+from helpers import oracle_fwd, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _dev(prob):
+    return prob.to(DEV)
+
+
+def _sync_ok():
+    torch.cuda.synchronize()
+    gb.check_device_error()
+
+
+# ---------------------------------------------------------------- workloads
+
+def test_pr1_fp16_mqa_causal():
+    prob = inputs.pr1()
+    o, lse = run_fwd(_dev(prob))
+    _sync_ok()
+    check_fwd(prob, o, lse)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.1])
+def test_page1_packed_views_equal_contiguous_and_oracle(scale):
+    prob = inputs.page1(scale=scale)
+    d = _dev(prob)
+    assert d.q.stride() == (1152, 1152, 64, 1)
+    o, lse = run_fwd(d)
+    qc, kc, vc = (t.contiguous() for t in (d.q, d.k, d.v))
+    oc, lsec = gb.attn_fwd(qc, kc, vc, **kw(d))
+    _sync_ok()
+    # same kernel, same tiles, same arithmetic: bitwise equal
+    assert torch.equal(o, oc) and torch.equal(lse, lsec)
+    check_fwd(prob, o, lse)
+
+
+def test_page3_fp32_forward_backward():
+    prob = inputs.page3()
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
+
+
+def test_page3_local_global_merge_equals_causal():
+    """Sliding-window-causal (band 64) over all rows, causal over the query
+    rows shifted by 65 (keys with q - kv > 64), merged by LSE on the shifted
+    rows: equals full causal attention (GPU vs GPU and vs oracle)."""
+    prob = inputs.page3()
+    d = _dev(prob)
+    band = 64
+    o_loc, l_loc = gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=(band, 0))
+    qg = d.q[:, band + 1:]
+    o_glb, l_glb = gb.attn_fwd(qg, d.k, d.v, scale=d.scale, window=(-1, 0))
+    o_m, l_m = gb.attn_merge_lse(o_loc[:, band + 1:], l_loc[:, :, band + 1:].contiguous(),
+                                 o_glb, l_glb)
+    o = torch.cat([o_loc[:, :band + 1], o_m], dim=1)
+    lse = torch.cat([l_loc[:, :, :band + 1], l_m], dim=2)
+    o_full, l_full = gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=(-1, 0))
+    _sync_ok()
+    causal = inputs.page3()
+    causal.window = (-1, 0)
+    check_fwd(causal, o, lse)
+    check_fwd(causal, o_full, l_full)
+    assert float((o - o_full).abs().max()) <= 1e-4
+
+
+def test_dense_bf16_s1024_d64_fwd_bwd():
+    prob = inputs.dense(8, 1024, 16, 64)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
+
+
+@pytest.mark.parametrize("S", [1024, 2048, 4096, 8192, 16384])
+def test_dense_bf16_sweep_d128_sampled(S):
+    """16384 tokens per batch at head dim 128, the bench's launch shapes;
+    compared on sampled rows (O, LSE, dq) and on the keys of two (batch, kv
+    head) units (dk, dv)."""
+    prob = inputs.dense(16384 // S, S, 16, 128)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    rows = sample_rows(prob, 48, seed=S)
+    check_fwd(prob, o, lse, row_sel=rows)
+    units = [(0, 0), (prob.B - 1, prob.Hkv - 1)]
+    keys = sample_keys(prob, units, 24, seed=S)
+    check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
+
+
+def test_varlen_thd_gqa_fwd_bwd_sampled():
+    prob = inputs.varlen()
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    rows = sample_rows(prob, 64)
+    check_fwd(prob, o, lse, row_sel=rows)
+    keys = sample_keys(prob, [(0, 0), (7, 3), (15, 7)], 24)
+    check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("case", [
+    dict(B=2, Sq=1, Skv=1, Hq=2, Hkv=1, window=(-1, 0)),
+    dict(B=1, Sq=17, Skv=17, Hq=3, Hkv=3, window=(-1, -1)),
+    dict(B=2, Sq=129, Skv=129, Hq=4, Hkv=2, window=(-1, 0)),
+    dict(B=1, Sq=200, Skv=77, Hq=2, Hkv=1, window=(-1, 0)),     # Sq > Skv, top-left
+    dict(B=1, Sq=70, Skv=300, Hq=2, Hkv=2, window=(-1, 0)),     # Sq < Skv
+    dict(B=1, Sq=300, Skv=300, Hq=4, Hkv=1, window=(40, 0)),    # sliding window
+    dict(B=1, Sq=260, Skv=260, Hq=2, Hkv=1, window=(5, 37)),    # two-sided window
+    dict(B=1, Sq=150, Skv=90, Hq=2, Hkv=1, window=(0, 0)),      # rows >= 90 see nothing
+])
+def test_edge_shapes_fwd_bwd(dtype, D, case):
+    prob = inputs.dense(case["B"], case["Sq"], case["Hq"], D, dtype=dtype,
+                        window=case["window"], Hkv=case["Hkv"], Skv=case["Skv"],
+                        seed=case["Sq"] + D)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
+
+
+@pytest.mark.parametrize("order", ["sbhd", "bhsd"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_layouts_equal_bshd(order, dtype):
+    """The same values stored as sbhd or bhsd give bitwise the same results
+    as bshd (strides are resolved by the kernels, never by copies)."""
+    a = inputs.random_case(5, B=2, Sq=192, Hq=4, Hkv=2, D=64, dtype=dtype, order="bshd")
+    b = inputs.random_case(5, B=2, Sq=192, Hq=4, Hkv=2, D=64, dtype=dtype, order=order)
+    da, db = _dev(a), _dev(b)
+    assert torch.equal(da.q, db.q) and da.q.stride() != db.q.stride()
+    oa, la = run_fwd(da)
+    ob, lb = run_fwd(db)
+    ga = run_bwd(da, oa, la)
+    gbb = run_bwd(db, ob, lb)
+    _sync_ok()
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+    for x, y in zip(ga, gbb):
+        assert torch.allclose(x.float(), y.float(), atol=0, rtol=0) or \
+            float((x.float() - y.float()).abs().max()) <= 2e-2 * float(x.float().abs().max())
+    check_fwd(a, oa, la)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_thd_with_empty_and_single_token_sequences(dtype):
+    prob = inputs.varlen(lengths=[1, 0, 129, 64, 300, 7], Hq=4, Hkv=2, D=64, dtype=dtype)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
+
+
+def test_thd_equals_dense_per_sequence():
+    """A THD pack gives, per sequence, exactly what the dense path gives for
+    that sequence alone (batch independence)."""
+    prob = inputs.varlen(lengths=[130, 257, 64], Hq=4, Hkv=2, D=128)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    cu = prob.cu_seqlens_q.tolist()
+    for b in range(3):
+        a, e = cu[b], cu[b + 1]
+        ob, lb = gb.attn_fwd(d.q[a:e][None], d.k[a:e][None], d.v[a:e][None],
+                             scale=d.scale, window=d.window)
+        assert torch.equal(ob[0], o[a:e])
+        assert torch.equal(lb[0], lse[:, a:e])
+    _sync_ok()
+
+
+def test_forward_is_deterministic():
+    prob = inputs.dense(2, 1000, 8, 128)
+    d = _dev(prob)
+    o1, l1 = run_fwd(d)
+    o2, l2 = run_fwd(d)
+    _sync_ok()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_packed_gradient_buffer_views():
+    """dq, dk, dv written into split views of one packed gradient buffer
+    (the layout of the page-1 inputs) match separate buffers."""
+    prob = inputs.page1(scale=0.1, seqlen=512)
+    d = _dev(prob)
+    dout = torch.randn(d.q.shape, generator=torch.Generator().manual_seed(3)).half().to(DEV)
+    o, lse = gb.attn_fwd(d.q, d.k, d.v, scale=0.1, window=(-1, 0))
+    g = torch.zeros_like(d.bases["qkv"])
+    gq, gk, gv = g.split([16, 1, 1], dim=2)
+    gq, gk, gv = (t.permute(1, 0, 2, 3) for t in (gq, gk, gv))
+    gb.attn_bwd(dout, d.q, d.k, d.v, o, lse, scale=0.1, window=(-1, 0), dq=gq, dk=gk, dv=gv)
+    dq, dk, dv = gb.attn_bwd(dout, d.q, d.k, d.v, o, lse, scale=0.1, window=(-1, 0))
+    _sync_ok()
+    assert torch.equal(gq, dq) and torch.equal(gk, dk) and torch.equal(gv, dv)
+
+
+# ---------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_merge_matches_oracle_with_empty_sides(dtype):
+    import oracle
+    g = torch.Generator().manual_seed(9)
+    B, S, H, D = 2, 100, 3, 128
+    o1 = torch.randn(B, S, H, D, generator=g).to(dtype)
+    o2 = torch.randn(B, S, H, D, generator=g).to(dtype)
+    l1 = torch.randn(B, H, S, generator=g) * 3
+    l2 = torch.randn(B, H, S, generator=g) * 3
+    l1[0, 0, :10] = -math.inf
+    l2[0, 0, 5:15] = -math.inf
+    o, l = gb.attn_merge_lse(o1.to(DEV), l1.to(DEV), o2.to(DEV), l2.to(DEV))
+    _sync_ok()
+    t = lambda x: to_f64(x).transpose(0, 2, 1, 3) if x.dim() == 4 else to_f64(x)
+    ro, rl = oracle.merge_lse(t(o1), t(l1), t(o2), t(l2))
+    tol = {torch.float16: 5e-3, torch.bfloat16: 1e-2, torch.float32: 1e-5}[dtype]
+    assert np.abs(t(o) - ro).max() <= tol
+    fin = np.isfinite(rl)
+    assert np.all(np.isneginf(to_f64(l))[~fin])
+    assert np.abs(to_f64(l)[fin] - rl[fin]).max() <= 1e-5
+
+
+def test_merge_in_place_and_thd():
+    g = torch.Generator().manual_seed(11)
+    T, H, D = 333, 4, 64
+    o1 = torch.randn(T, H, D, generator=g).bfloat16().to(DEV)
+    o2 = torch.randn(T, H, D, generator=g).bfloat16().to(DEV)
+    l1 = torch.randn(H, T, generator=g).to(DEV)
+    l2 = torch.randn(H, T, generator=g).to(DEV)
+    ref_o, ref_l = gb.attn_merge_lse(o1, l1, o2, l2)
+    gb.attn_merge_lse(o1, l1, o2, l2, out=o1, lse_out=l1)
+    _sync_ok()
+    assert torch.equal(o1, ref_o) and torch.equal(l1, ref_l)
+
+
+# ---------------------------------------------------------------- watchdog
+
+def test_watchdog_gives_up_and_reports():
+    """A wait on a barrier nothing arrives on ends after the limit with an
+    error the host reads; the context stays usable."""
+    old = gb.set_watchdog_ns(2_000_000)  # 2 ms
+    try:
+        gb.watchdog_selftest()
+        with pytest.raises(gb.AttnError) as ei:
+            gb.check_device_error()
+        assert ei.value.status == 4
+    finally:
+        gb.set_watchdog_ns(old)
+    gb.check_device_error()  # cleared
+    prob = inputs.pr1()
+    o, lse = run_fwd(_dev(prob))
+    _sync_ok()
+    check_fwd(prob, o, lse)
