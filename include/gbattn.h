@@ -111,7 +111,7 @@ typedef struct {
     const int32_t *cu_seqlens_kv; /* offsets starting at 0 (NULL for DENSE4D) */
     int max_seqlen_q;    /* THD only: upper bound of the sequence lengths */
     int max_seqlen_kv;
-    float scale;         /* softmax scale, e.g. 1/sqrt(D) */
+    float scale;         /* softmax scale, finite and > 0, e.g. 1/sqrt(D) */
     int window_left;     /* -1 = unbounded */
     int window_right;    /* -1 = unbounded; (-1, 0) = causal */
 } attn_params;

@@ -77,7 +77,8 @@ attn_status check_params(const attn_params *p) {
     if (p->window_left < -1 || p->window_right < -1)
         return fail(ATTN_ERR_INVALID_ARG, "window (%d, %d): each bound must be >= -1",
                     p->window_left, p->window_right);
-    if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
+    if (!std::isfinite(p->scale) || !(p->scale > 0.f))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and positive");
     if (p->layout == ATTN_LAYOUT_THD) {
         if (p->B > 0 && (!p->cu_seqlens_q || !p->cu_seqlens_kv))
             return fail(ATTN_ERR_INVALID_ARG, "THD layout needs cu_seqlens_q and cu_seqlens_kv");

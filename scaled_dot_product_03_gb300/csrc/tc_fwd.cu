@@ -1,13 +1,404 @@
-// tc_fwd.cu -- tcgen05 forward kernel (fp16/bf16).
+// tc_fwd.cu -- tcgen05 forward attention for fp16 / bf16 (head dim 64, 128).
+//
+// One CTA owns two 128-row query tiles of one (batch, query head) and walks
+// the key/value blocks of 128 rows that any of its rows can see (causal and
+// window masks are resolved per block: blocks nobody sees are never loaded,
+// blocks everybody sees are never masked).  Per block and tile:
+//
+//   S = Q K^T           tcgen05.mma, Q and K from shared memory (TMA, 128B
+//                       swizzle), fp32 accumulator in tensor memory (TMEM)
+//   online softmax      one thread per row: row max, exp2, row sum, P rounded
+//                       to the input type and written back over S in TMEM;
+//                       O is rescaled only when the running max grows by more
+//                       than 2^8 (exact: the same reference max is used for P,
+//                       l and O, and the final O / l cancels it)
+//   O += P V            tcgen05.mma with P read from TMEM, V from shared memory
+//
+// Warp roles (320 threads): warps 0-3 softmax + epilogue of tile 0, warps 4-7
+// the same for tile 1, warp 8 issues TMA loads, warp 9 allocates TMEM and
+// issues the MMAs.  Tiles are handed between roles with mbarriers; every wait
+// is bounded by the watchdog.
+//
+// TMEM columns (512 allocated): S/P of tile 0 at 0, of tile 1 at 128; O of
+// tile 0 at 256, of tile 1 at 256 + D.
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "tc.h"
+#include "tmap.h"
 
 namespace gbattn {
+namespace {
 
-bool uses_tc_fwd(int dtype, int D) { return false; }
+using namespace ptx;
+
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 128;          // keys per block
+constexpr int NQ = 2;            // query tiles per CTA
+constexpr int kThreads = 320;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kChunks = D / 64;                 // 64-element swizzle atoms per row
+    static constexpr int kTileBytes = BM * D * 2;          // one 128 x D tile
+    static constexpr int kStages = D == 128 ? 2 : 3;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + NQ * kTileBytes;
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+    uint64_t s_full[NQ], p_full[NQ], pv_done[NQ];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Key-block range of one query tile, in blocks relative to the CTA's first key.
+struct TileRange {
+    int row0;     // first query row of the tile
+    int nrows;    // valid rows (0 if the tile lies past the sequence)
+    int blo, bhi; // blocks [blo, bhi)
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, FwdArgs a, int n_mtiles) {
+    using C = FwdCfg<D>;
+    constexpr int KS = C::kStages;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    Bars &bar = *reinterpret_cast<Bars *>(smem + C::kBarOff);
+    const Geometry &g = a.g;
+
+    // heaviest tiles (largest row index) first across all heads and batches
+    const int bh = blockIdx.x % (g.Hq * g.B);
+    const int mt = n_mtiles - 1 - (int)(blockIdx.x / (g.Hq * g.B));
+    const int h = bh % g.Hq, b = bh / g.Hq;
+    const int hk = h / g.G;
+    const SeqInfo s = seq_info(g, b);
+    const int m0 = mt * (BM * NQ);
+    if (m0 >= s.Lq) return;
+
+    // key range of the CTA and of each tile
+    int jlo, jhi;
+    key_range(m0, min(m0 + BM * NQ, s.Lq), s.Lkv, g.wl, g.wr, jlo, jhi);
+    const int nb = (jhi - jlo + BN - 1) / BN;
+    TileRange tr[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+        tr[i].row0 = m0 + i * BM;
+        tr[i].nrows = max(0, min(BM, s.Lq - tr[i].row0));
+        tr[i].blo = tr[i].bhi = 0;
+        if (tr[i].nrows > 0) {
+            int lo, hi;
+            key_range(tr[i].row0, tr[i].row0 + tr[i].nrows, s.Lkv, g.wl, g.wr, lo, hi);
+            if (hi > lo) {
+                tr[i].blo = (lo - jlo) / BN;
+                tr[i].bhi = (hi - jlo + BN - 1) / BN;
+            }
+        }
+    }
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar.q_full, 1);
+        for (int i = 0; i < KS; ++i) {
+            mbar_init(&bar.k_full[i], 1);
+            mbar_init(&bar.k_empty[i], 1);
+            mbar_init(&bar.v_full[i], 1);
+            mbar_init(&bar.v_empty[i], 1);
+        }
+        for (int i = 0; i < NQ; ++i) {
+            mbar_init(&bar.s_full[i], 1);
+            mbar_init(&bar.p_full[i], BM);
+            mbar_init(&bar.pv_done[i], 1);
+        }
+        bar.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bar.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == kProdWarp && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+    const Watchdog wd{a.watchdog_ns, a.err, &bar.abort_flag};
+
+    const uint32_t sQ = smem_u32(smem + C::kQOff);
+    const uint32_t sK = smem_u32(smem + C::kKOff);
+    const uint32_t sV = smem_u32(smem + C::kVOff);
+    // TMA coordinates: (d, row, head, batch); THD views have one "batch"
+    const int qb = g.thd ? 0 : b, q_row = s.q0 + m0;
+    const int kv_row = s.kv0 + jlo;
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0 && nb > 0) {
+            mbar_arrive_expect_tx(&bar.q_full, NQ * C::kTileBytes);
+            for (int i = 0; i < NQ; ++i)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(smem + C::kQOff + i * C::kTileBytes + c * BM * 128, &tm_q,
+                                &bar.q_full, c * 64, q_row + i * BM, h, qb);
+            for (int jb = 0; jb < nb; ++jb) {
+                const int st = jb % KS;
+                const uint32_t ph = (jb / KS) & 1;
+                if (!mbar_wait(&bar.k_empty[st], ph ^ 1, wd, 0x10)) break;
+                mbar_arrive_expect_tx(&bar.k_full[st], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(smem + C::kKOff + st * C::kTileBytes + c * BN * 128, &tm_k,
+                                &bar.k_full[st], c * 64, kv_row + jb * BN, hk, qb);
+                if (!mbar_wait(&bar.v_empty[st], ph ^ 1, wd, 0x11)) break;
+                mbar_arrive_expect_tx(&bar.v_full[st], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(smem + C::kVOff + st * C::kTileBytes + c * BN * 128, &tm_v,
+                                &bar.v_full[st], c * 64, kv_row + jb * BN, hk, qb);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && nb > 0) {
+            constexpr uint32_t idS = idesc_f16(BM, BN, kBf16, 0, 0);
+            constexpr uint32_t idPV = idesc_f16(BM, D, kBf16, 0, 1);
+            bool ok = mbar_wait(&bar.q_full, 0, wd, 0x20);
+            for (int jb = 0; ok && jb < nb; ++jb) {
+                const int st = jb % KS;
+                const uint32_t ph = (jb / KS) & 1;
+                if (!(ok = mbar_wait(&bar.k_full[st], ph, wd, 0x21))) break;
+                tc_fence_after();
+                for (int i = 0; i < NQ; ++i) {
+                    if (jb < tr[i].blo || jb >= tr[i].bhi) continue;
+                    const int t = jb - tr[i].blo;
+                    // S_i still holds P of the previous block until that PV is done
+                    if (t > 0 && !(ok = mbar_wait(&bar.pv_done[i], (t - 1) & 1, wd, 0x22))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        const uint64_t da = smem_desc_sw128(sQ + i * C::kTileBytes + off, 16, 1024);
+                        const uint64_t db = smem_desc_sw128(sK + st * C::kTileBytes + off, 16, 1024);
+                        mma_ss(tmem + i * BN, da, db, idS, kk > 0);
+                    }
+                    mma_commit(&bar.s_full[i]);
+                }
+                if (!ok) break;
+                mma_commit(&bar.k_empty[st]);
+                if (!(ok = mbar_wait(&bar.v_full[st], ph, wd, 0x23))) break;
+                tc_fence_after();
+                for (int i = 0; i < NQ; ++i) {
+                    if (jb < tr[i].blo || jb >= tr[i].bhi) continue;
+                    const int t = jb - tr[i].blo;
+                    if (!(ok = mbar_wait(&bar.p_full[i], t & 1, wd, 0x24))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t db = smem_desc_sw128(sV + st * C::kTileBytes + kk * 16 * 128,
+                                                            BN * 128, 1024);
+                        mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8, db, idPV,
+                               (t > 0 || kk > 0));
+                    }
+                    mma_commit(&bar.pv_done[i]);
+                }
+                if (!ok) break;
+                mma_commit(&bar.v_empty[st]);
+            }
+        }
+    } else {
+        // ------------------------------------------------- softmax + epilogue
+        const int i = warp / 4;          // tile
+        const int wq = warp % 4;         // TMEM lane quarter
+        const int r = wq * 32 + lane;    // row within the tile
+        const int row = tr[i].row0 + r;  // row within the sequence
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + i * BN + lane_off;
+        const uint32_t tO = tmem + 2 * BN + i * D + lane_off;
+        const int n_i = tr[i].bhi - tr[i].blo;
+        const float c2 = g.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < n_i; ++t) {
+            const int jb = tr[i].blo + t;
+            const int n0 = jlo + jb * BN;  // first key of the block
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[i], t & 1, wd, 0x30));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[BN];
+            tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+            tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+            // mask only blocks that some row of the tile sees only in part
+            const int rlo = tr[i].row0, rhi = tr[i].row0 + tr[i].nrows - 1;
+            const bool full = (n0 + BN - 1 < s.Lkv) && (g.wr < 0 || n0 + BN - 1 <= rlo + g.wr) &&
+                              (g.wl < 0 || n0 >= rhi - g.wl);
+            float mx = -INFINITY;
+            if (full) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    if (!visible(row, n0 + c, s.Lkv, g.wl, g.wr)) sr[c] = __float_as_uint(-INFINITY);
+                    mx = fmaxf(mx, __uint_as_float(sr[c]));
+                }
+            }
+            const float xm = mx * c2;  // scale > 0, so the max commutes with scaling
+            float alpha = 1.f;
+            bool resc = false;
+            if (xm > m + kRescaleThreshold) {  // also the first visible block (m = -inf)
+                alpha = ex2(m - xm);
+                m = xm;
+                resc = true;
+            }
+            const float mref = m == -INFINITY ? 0.f : m;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 2; ++c) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), c2, -mref));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), c2, -mref));
+                rs += p0 + p1;
+                sr[c] = pack2<T>(p0, p1);
+            }
+            l = l * alpha + rs;
+            tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            // O holds the blocks before this one (their PV completed before
+            // this block's S was issued); rescale it when some row's max moved.
+            if (t > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + cc * 32, ov);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(tO + cc * 32, ov);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar.p_full[i]);
+        }
+        // epilogue: O / l -> global, LSE
+        if (ok && n_i > 0)
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.pv_done[i], (n_i - 1) & 1, wd, 0x31));
+        tc_fence_after();
+        const bool valid = r < tr[i].nrows;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T *orow = (T *)a.o.ptr + (int64_t)b * a.o.sb + (int64_t)(s.q0 + row) * a.o.ss +
+                  (int64_t)h * a.o.sh;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            if (n_i > 0) {
+                tmem_ld32(tO + cc * 32, ov);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ov[e] = 0u;
+            }
+            if (valid) {
+                uint4 pk[4];
+                uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pw[e] = pack2<T>(__uint_as_float(ov[2 * e]) * inv,
+                                     __uint_as_float(ov[2 * e + 1]) * inv);
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = pk[e];
+            }
+        }
+        if (valid)
+            a.lse[lse_index(g, s, b, h, row)] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
+    const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+    const Geometry &g = a.g;
+    CUtensorMap tq, tk, tv;
+    const uint64_t es = 2;
+    // dims (d, rows, heads, batch); THD: rows = all tokens, one batch
+    const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
+    uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
+    uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
+    // byte strides of (rows, heads, batch); a size-1 dim may carry any stride
+    auto strides = [&](const View &v, const uint64_t dims[4], uint64_t out[3]) {
+        const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
+        for (int i = 0; i < 3; ++i)
+            out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
+    };
+    uint64_t sq[3], sk[3], sv[3];
+    strides(a.q, dq, sq);
+    strides(a.k, dk, sk);
+    strides(a.v, dk, sv);
+    cudaError_t e;
+    if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BM)) != cudaSuccess) return e;
+    if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BN)) != cudaSuccess) return e;
+    const int smem = FwdCfg<D>::kSmemBytes;
+    auto kern = tc_fwd_kernel<T, D>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+        cudaSuccess)
+        return e;
+    const int n_mtiles = (max_lq + BM * NQ - 1) / (BM * NQ);
+    const int64_t grid = (int64_t)n_mtiles * g.Hq * g.B;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, a, n_mtiles);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool uses_tc_fwd(int dtype, int D) { return (dtype == 0 || dtype == 1) && (D == 64 || D == 128); }
 
 cudaError_t launch_tc_fwd(int dtype, const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
-    return cudaErrorNotSupported;
+    switch (dtype * 2 + (a.g.D == 128)) {
+        case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, st);
+        case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, st);
+        case 2: return launch_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, st);
+        case 3: return launch_typed<__nv_bfloat16, 128>(a, max_lq, max_lkv, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gbattn

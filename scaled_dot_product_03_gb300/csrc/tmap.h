@@ -1,0 +1,17 @@
+// tmap.h -- TMA tensor maps built from the caller's strides (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbattn {
+
+// 4-D tiled tensor map over a (d, s, h, b) view of 16-bit elements
+// (dtype 0 = fp16, 1 = bf16), 128-byte swizzle, box {64, box_rows, 1, 1}.
+// dims are element counts innermost first, strides_bytes are the byte
+// strides of dims 1..3 (each a multiple of 16).  Out-of-range rows read as 0.
+cudaError_t make_tmap_16bit(CUtensorMap *map, const void *ptr, int dtype, const uint64_t dims[4],
+                            const uint64_t strides_bytes[3], uint32_t box_rows);
+
+}  // namespace gbattn

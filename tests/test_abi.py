@@ -65,6 +65,8 @@ def _t(ptr=4096, strides=(32768, 256, 64, 1)):
     (dict(layout=5), _lib.ATTN_ERR_INVALID_ARG),
     (dict(B=-1), _lib.ATTN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-0.5), _lib.ATTN_ERR_INVALID_ARG),
     (dict(layout=_lib.ATTN_LAYOUT_THD), _lib.ATTN_ERR_INVALID_ARG),  # no cu_seqlens
 ])
 def test_invalid_params_rejected_without_launch(lib, kw, status):
