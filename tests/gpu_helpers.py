@@ -48,7 +48,8 @@ def lse_rows(prob, lse):
 
 
 def max_abs(a, b, mask=None):
-    d = np.abs(a - b)
+    with np.errstate(invalid="ignore"):  # -inf - -inf outside the mask
+        d = np.abs(a - b)
     if mask is not None:
         d = d[mask]
     return float(d.max()) if d.size else 0.0
