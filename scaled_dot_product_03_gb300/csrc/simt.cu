@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 
 // ---------------------------------------------------------------------------
 // Backward preprocess: delta = <dO, O> per (row, head); one warp per pair.
+// Also clears the fp32 dq accumulator when the backward uses one.
 template <typename T>
 __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
     const Geometry &g = a.g;
@@ -130,6 +131,10 @@ __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
         }
         const T *o = row_ptr<T>(a.o, b, row, h);
         const T *d_o = row_ptr<T>(a.dout, b, row, h);
+        if (a.dq_acc) {  // the tensor-core backward accumulates dq here
+            float *acc_row = a.dq_acc + ((int64_t)r * g.Hq + h) * g.D;
+            for (int d = lane; d < g.D; d += 32) acc_row[d] = 0.f;
+        }
         float acc = 0.f;
         for (int d = lane; d < g.D; d += 32) acc = fmaf(to_f32(o[d]), to_f32(d_o[d]), acc);
 #pragma unroll
