@@ -173,6 +173,40 @@ GBATTN_API attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int
                            const float *lse2, attn_tensor o_out,
                            float *lse_out, attn_stream_t stream);
 
+/*
+ * attn_bwd without a caller-provided workspace.  (The source pages have no
+ * counterpart: this entry point exists for callers of the library, not for
+ * the method.)
+ *
+ * Some callers cannot allocate device memory at the point where they run the
+ * backward pass: code that owns no allocator (a plugin or foreign-language
+ * host handed only tensor pointers), or code that must not allocate once its
+ * set-up is over.  This variant takes the same arguments as attn_bwd minus
+ * the workspace and uses a fixed scratch array that the library itself holds
+ * in device memory: GBATTN_NOALLOC_SCRATCH_BYTES bytes, reserved on every GPU
+ * that loads this part of the library and held until the process exits.  It
+ * never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Limits and behaviour:
+ *   - Problems whose attn_bwd_workspace_size exceeds the scratch size are
+ *     rejected with ATTN_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on each device looks up the device address of the
+ *     scratch (with that device current); make that first call before any
+ *     stream capture begins.
+ *   - Every call, on every stream, shares the one scratch array, which keeps
+ *     the previous call's contents (each call clears what it needs cleared).
+ *     Calls whose work may overlap on the GPU (different streams without
+ *     ordering between them) race on the scratch and give wrong gradients;
+ *     serialise them.
+ */
+#define GBATTN_NOALLOC_SCRATCH_BYTES (64u << 20)
+GBATTN_API attn_status attn_bwd_noalloc(const attn_params *p, attn_tensor q,
+                                        attn_tensor k, attn_tensor v,
+                                        attn_tensor o, attn_tensor dout,
+                                        const float *lse, attn_tensor dq,
+                                        attn_tensor dk, attn_tensor dv,
+                                        attn_stream_t stream);
+
 /* Description of the calling thread's last failure ("" if none). */
 GBATTN_API const char *attn_last_error_string(void);
 

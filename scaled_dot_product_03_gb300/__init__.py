@@ -19,7 +19,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_merge_lse", "attn_bwd_workspace_size",
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_merge_lse", "attn_bwd_workspace_size",
            "check_device_error", "set_watchdog_ns", "watchdog_selftest", "AttnError",
            "params_for"]
 
@@ -144,6 +144,33 @@ def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens
                             _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd),
                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                             _stream(q)))
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1),
+                     cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None,
+                     max_seqlen_kv=None, dq=None, dk=None, dv=None
+                     ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """:func:`attn_bwd` for callers that cannot allocate device scratch: the
+    library's own fixed scratch array (``_lib.NOALLOC_SCRATCH_BYTES`` bytes per
+    device) replaces the workspace.  Calls share that array, so calls that
+    could overlap on the GPU must be serialised.  (This wrapper still lets
+    torch allocate dq/dk/dv when they are not passed.)"""
+    p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
+                   cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
+                   max_seqlen_kv=max_seqlen_kv)
+    thd = p.layout == _lib.ATTN_LAYOUT_THD
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty(k.shape, dtype=k.dtype, device=k.device)
+    if dv is None:
+        dv = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    lib = _lib.load()
+    _lib.check(lib.attn_bwd_noalloc(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                                    _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
+                                    _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd),
+                                    _stream(q)))
     return dq, dk, dv
 
 

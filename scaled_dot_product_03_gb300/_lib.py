@@ -21,7 +21,8 @@ ATTN_LAYOUT_DENSE4D, ATTN_LAYOUT_THD = 0, 1
 # Every symbol include/gbattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_merge_lse",
            "attn_last_error_string", "attn_check_device_error", "attn_set_watchdog_ns",
-           "attn_watchdog_selftest")
+           "attn_watchdog_selftest", "attn_bwd_noalloc")
+NOALLOC_SCRATCH_BYTES = 64 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 
 class AttnTensor(ctypes.Structure):
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
         lib.attn_set_watchdog_ns.restype = ctypes.c_uint64
         lib.attn_watchdog_selftest.argtypes = [S]
         lib.attn_watchdog_selftest.restype = i32
+        lib.attn_bwd_noalloc.argtypes = [P, T, T, T, T, T, f32p, T, T, T, S]
+        lib.attn_bwd_noalloc.restype = i32
         _lib = lib
         return lib
 

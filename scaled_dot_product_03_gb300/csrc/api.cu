@@ -174,6 +174,12 @@ WsLayout ws_layout(const attn_params *p) {
 }
 
 }  // namespace
+
+attn_status record_error(attn_status st, const char *msg) {
+    t_error = msg;
+    return st;
+}
+
 }  // namespace gbattn
 
 using namespace gbattn;
