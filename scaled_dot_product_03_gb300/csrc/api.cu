@@ -6,7 +6,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/gbattn.h"
+#include "gbattn.h"
 #include "launch.h"
 #include "tc.h"
 

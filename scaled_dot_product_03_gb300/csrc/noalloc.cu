@@ -10,7 +10,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/gbattn.h"
+#include "gbattn.h"
 
 namespace {
 

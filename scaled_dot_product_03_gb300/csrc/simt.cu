@@ -110,36 +110,52 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward preprocess: delta = <dO, O> per (row, head); one warp per pair.
-// Also clears the fp32 dq accumulator when the backward uses one.
-template <typename T>
+// Backward preprocess: delta = <dO, O> per (row, head).  A group of up to 32
+// lanes (power of two) covers one (row, head), each lane VEC elements at a
+// time.  Also clears the fp32 dq accumulator ([Hq][rows][D]) when the
+// backward uses one.
+template <typename T, int VEC>
 __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
+    struct alignas(sizeof(T) * VEC) Vt { T v[VEC]; };
     const Geometry &g = a.g;
-    const int lane = threadIdx.x & 31;
+    const int D = g.D;
+    const int chunks = D / VEC;
+    const int tpr = chunks < 32 ? chunks : 32;
+    const int lane = threadIdx.x & 31, sub = lane / tpr, c0 = lane % tpr;
+    const int per_warp = 32 / tpr;
+    const int64_t pairs = (int64_t)rows * g.Hq;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-         w < (int64_t)rows * g.Hq; w += nwarps) {
-        const int r = (int)(w / g.Hq), h = (int)(w % g.Hq);
-        int b = 0, row = r;
-        int64_t idx;
-        if (g.thd) {
-            idx = (int64_t)h * g.Tq + r;
-        } else {
-            b = r / g.Sq;
-            row = r % g.Sq;
-            idx = ((int64_t)b * g.Hq + h) * g.Sq + row;
-        }
-        const T *o = row_ptr<T>(a.o, b, row, h);
-        const T *d_o = row_ptr<T>(a.dout, b, row, h);
-        if (a.dq_acc) {  // the tensor-core backward accumulates dq here
-            float *acc_row = a.dq_acc + ((int64_t)r * g.Hq + h) * g.D;
-            for (int d = lane; d < g.D; d += 32) acc_row[d] = 0.f;
-        }
+         w * per_warp < pairs; w += nwarps) {
+        const int64_t pr = w * per_warp + sub;
+        const bool active = pr < pairs;
         float acc = 0.f;
-        for (int d = lane; d < g.D; d += 32) acc = fmaf(to_f32(o[d]), to_f32(d_o[d]), acc);
+        int64_t idx = 0;
+        if (active) {
+            const int r = (int)(pr / g.Hq), h = (int)(pr % g.Hq);
+            int b = 0, row = r;
+            if (g.thd) {
+                idx = (int64_t)h * g.Tq + r;
+            } else {
+                b = r / g.Sq;
+                row = r % g.Sq;
+                idx = ((int64_t)b * g.Hq + h) * g.Sq + row;
+            }
+            const Vt *o = reinterpret_cast<const Vt *>(row_ptr<T>(a.o, b, row, h));
+            const Vt *d_o = reinterpret_cast<const Vt *>(row_ptr<T>(a.dout, b, row, h));
+            float *acc_row = a.dq_acc ? a.dq_acc + ((int64_t)h * rows + r) * D : nullptr;
+            for (int c = c0; c < chunks; c += tpr) {
+                const Vt x = o[c], y = d_o[c];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) a.delta[idx] = acc;
+                for (int e = 0; e < VEC; ++e) acc = fmaf(to_f32(x.v[e]), to_f32(y.v[e]), acc);
+                if (acc_row) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc_row[c * VEC + e] = 0.f;
+                }
+            }
+        }
+        for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (active && c0 == 0) a.delta[idx] = acc;
     }
 }
 
@@ -359,15 +375,32 @@ cudaError_t launch_simt_fwd(int dtype, const FwdArgs &a, int max_lq, cudaStream_
     return cudaErrorInvalidValue;
 }
 
+namespace {
+bool rows_aligned16(const View &v, size_t es) {
+    return ((uintptr_t)v.ptr % 16) == 0 && (v.sb * es) % 16 == 0 && (v.ss * es) % 16 == 0 &&
+           (v.sh * es) % 16 == 0;
+}
+template <typename T, int VEC>
+void preprocess_typed(const BwdArgs &a, int rows, cudaStream_t st) {
+    const int tpr = (a.g.D / VEC) < 32 ? a.g.D / VEC : 32;
+    const int64_t warps = ((int64_t)rows * a.g.Hq + (32 / tpr) - 1) / (32 / tpr);
+    int64_t blocks = (warps + 7) / 8;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    bwd_preprocess_kernel<T, VEC><<<(unsigned)blocks, 256, 0, st>>>(a, rows);
+}
+}  // namespace
+
 cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStream_t st) {
-    const int64_t work = (int64_t)rows * a.g.Hq;
-    const int threads = 256;
-    const int64_t blocks = (work + 7) / 8;
-    const int grid = (int)(blocks < 152 * 32 ? (blocks < 1 ? 1 : blocks) : 152 * 32);
     switch (dtype) {
-        case 0: bwd_preprocess_kernel<__half><<<grid, threads, 0, st>>>(a, rows); break;
-        case 1: bwd_preprocess_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(a, rows); break;
-        case 2: bwd_preprocess_kernel<float><<<grid, threads, 0, st>>>(a, rows); break;
+        case 0: preprocess_typed<__half, 8>(a, rows, st); break;
+        case 1: preprocess_typed<__nv_bfloat16, 8>(a, rows, st); break;
+        case 2:
+            if (rows_aligned16(a.o, 4) && rows_aligned16(a.dout, 4))
+                preprocess_typed<float, 4>(a, rows, st);
+            else
+                preprocess_typed<float, 1>(a, rows, st);
+            break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

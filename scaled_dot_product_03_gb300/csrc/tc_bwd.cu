@@ -12,7 +12,9 @@
 //   dV  += P^T dO           P^T rounded to the input type, read from TMEM
 //   dK  += dS^T Q           dS^T read from TMEM
 //   dQ^T = K^T dS^T         dS^T also written to shared memory; the result is
-//                           added to an fp32 dq accumulator in global memory
+//                           staged in shared memory and added to an fp32 dq
+//                           accumulator in global memory by one bulk
+//                           reduction per block
 //
 // (dK and dQ are scaled once at the end.)  Warp roles (320 threads): warps
 // 0-3 compute P and dS (thread = key row) and store dK, dV at the end;
@@ -49,7 +51,8 @@ struct BwdCfg {
     static constexpr int kDOOff = kQOff + QS * kQBytes;
     static constexpr int kDSOff = kDOOff + QS * kQBytes;     // dS^T [128 keys][64 q]
     static constexpr int kZeroOff = kDSOff + BN * BMQ * 2;   // zero tile (D = 64 only)
-    static constexpr int kStatOff = kZeroOff + (D == 64 ? BN * 128 : 0);
+    static constexpr int kDQOff = kZeroOff + (D == 64 ? BN * 128 : 0);  // fp32 [64 q][D]
+    static constexpr int kStatOff = kDQOff + BMQ * D * 4;
     static constexpr int kBarOff = kStatOff + QS * BMQ * 2 * 4;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;
     // TMEM columns
@@ -60,7 +63,7 @@ struct BwdCfg {
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[QS], q_empty[QS];
-    uint64_t s_full, dp_full, ds_full, it_done, dq_empty;
+    uint64_t s_full, dp_full, ds_full, dk_done, it_done, dq_empty;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -81,8 +84,20 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void red_add_f32(float *addr, float v) {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+// global[0 .. bytes) += shared[0 .. bytes) (fp32), as one bulk operation.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                     gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 template <typename T, int D>
@@ -122,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.dp_full, 1);
         mbar_init(&bar.ds_full, 128);
+        mbar_init(&bar.dk_done, 1);
         mbar_init(&bar.it_done, 1);
         mbar_init(&bar.dq_empty, 128);
         bar.abort_flag = 0;
@@ -226,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = t % QS;
                 const uint32_t sq = sQ + st * C::kQBytes, sdo = sDO + st * C::kQBytes;
                 // dP^T into the dP buffer, free once iteration t-1's dK finished
-                if (t > 0 && !(ok = mbar_wait(&bar.it_done, (t - 1) & 1, wd, 0x52))) break;
+                if (t > 0 && !(ok = mbar_wait(&bar.dk_done, (t - 1) & 1, wd, 0x52))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -236,6 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                            smem_desc_sw128(sdo + offb, 16, 1024), idSP, kk > 0);
                 }
                 mma_commit(&bar.dp_full);
+                // S^T of the next block runs while P and dS of this one are made
+                // (its buffer held P of block t-1, whose dV finished before dk_done)
+                if (t + 1 < n_it) {
+                    if (!(ok = mbar_wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, wd, 0x55)))
+                        break;
+                    tc_fence_after();
+                    issue_s(t + 1);
+                }
                 if (!(ok = mbar_wait(&bar.ds_full, t & 1, wd, 0x53))) break;
                 tc_fence_after();
                 // dV += P^T dO, dK += dS^T Q  (B operands MN-major: N = head dim)
@@ -252,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (t > 0 || kk > 0));
                 }
                 mma_commit(&bar.q_empty[st]);
+                mma_commit(&bar.dk_done);
                 // dQ^T = K^T dS^T into the dQ buffer, free once drained
                 if (t > 0 && !(ok = mbar_wait(&bar.dq_empty, (t - 1) & 1, wd, 0x54))) break;
                 tc_fence_after();
@@ -261,12 +286,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                            smem_desc_sw128(sDS + kk * 16 * 128, BN * 128, 1024), idQ, kk > 0);
                 }
                 mma_commit(&bar.it_done);
-                if (t + 1 < n_it) {
-                    if (!(ok = mbar_wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, wd, 0x55)))
-                        break;
-                    tc_fence_after();
-                    issue_s(t + 1);
-                }
             }
         }
     } else if (warp < 4) {
@@ -373,10 +392,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------- dQ^T drain (thread = head dim)
+        // dq accumulator layout: [Hq][rows][D] fp32, so the block's rows of one
+        // head are contiguous and go out as a single bulk reduction.
         const int wq = warp % 4;
         const int d = wq * 32 + lane;
         const uint32_t tQ = tmem + C::kTmDQ + ((uint32_t)(wq * 32) << 16);
         const bool has = wq * 32 < D;  // D = 64: lanes 64..127 hold zeros
+        const bool leader = threadIdx.x == 128;
+        float *sdq = reinterpret_cast<float *>(smem + C::kDQOff);
+        const int64_t rows_total = g.thd ? (int64_t)g.Tq : (int64_t)g.B * g.Sq;
+        const int64_t row_base = g.thd ? s.q0 : (int64_t)b * g.Sq;
         for (int t = 0; t < n_it; ++t) {
             const int h = hk * g.G + t / nqb;
             const int i0 = ilo + (t % nqb) * BMQ;
@@ -389,14 +414,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&bar.dq_empty);
+            if (leader) bulk_wait_read0();  // previous block's staging tile was read
+            named_bar_sync(1, 128);
             if (has) {
+#pragma unroll
+                for (int c = 0; c < BMQ; ++c) sdq[c * D + d] = __uint_as_float(v[c]);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (leader) {
                 const int nrow = min(BMQ, s.Lq - i0);
-                float *base = a.dq_acc + ((int64_t)(s.q0 + (g.thd ? 0 : b * g.Sq) + i0) * g.Hq + h) * D + d;
-#pragma unroll 8
-                for (int c = 0; c < BMQ; ++c)
-                    if (c < nrow) red_add_f32(base + (int64_t)c * g.Hq * D, __uint_as_float(v[c]));
+                float *dst = a.dq_acc + ((int64_t)h * rows_total + row_base + i0) * D;
+                bulk_reduce_add_f32(dst, sdq, (uint32_t)(nrow * D * 4));
+                bulk_commit();
             }
         }
+        if (leader) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
@@ -407,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// dq = scale * dq_acc, converted and written through dq's strides.
+// dq = scale * dq_acc ([Hq][rows][D] fp32), converted and written through
+// dq's strides.
 template <typename T>
 __global__ void dq_convert_kernel(BwdArgs a, int rows) {
     const Geometry &g = a.g;
@@ -416,15 +450,15 @@ __global__ void dq_convert_kernel(BwdArgs a, int rows) {
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x) {
         const int c8 = (int)(e % (D / 8));
-        const int64_t rh = e / (D / 8);
-        const int h = (int)(rh % g.Hq);
-        const int r = (int)(rh / g.Hq);
+        const int64_t hr = e / (D / 8);  // h * rows + r
+        const int r = (int)(hr % rows);
+        const int h = (int)(hr / rows);
         int b = 0, row = r;
         if (!g.thd) {
             b = r / g.Sq;
             row = r % g.Sq;
         }
-        const float4 *src = reinterpret_cast<const float4 *>(a.dq_acc + rh * D + c8 * 8);
+        const float4 *src = reinterpret_cast<const float4 *>(a.dq_acc + hr * D + c8 * 8);
         const float4 x = src[0], y = src[1];
         uint4 o;
         o.x = pack2<T>(x.x * g.scale, x.y * g.scale);
