@@ -16,13 +16,17 @@
 //                           accumulator in global memory by one bulk
 //                           reduction per block
 //
-// (dK and dQ are scaled once at the end.)  Warp roles (320 threads): warps
-// 0-3 compute P and dS (thread = key row) and store dK, dV at the end;
-// warps 4-7 drain dQ^T from TMEM into the global accumulator (thread = head
-// dim); warp 8 issues TMA loads; warp 9 allocates TMEM and issues the MMAs.
+// (dK and dQ are scaled once at the end.)  Warp roles (448 threads): warps
+// 0-7 compute P and dS (thread = key row; warps 0-3 take query columns 0-31,
+// warps 4-7 columns 32-63) and store dK (0-3) and dV (4-7) at the end; warps
+// 8-11 drain dQ^T from TMEM into the global accumulator (thread = head dim);
+// warp 12 issues the loads (query blocks run QS stages ahead); warp 13
+// allocates TMEM and issues the MMAs.
 //
 // TMEM columns: dK [0, D), dV [D, 2D), S/P double buffer 2 x 64, dP/dS 64,
 // dQ^T 64 (M = 128 rows; for D = 64 the upper 64 rows multiply a zero tile).
+// P and dS overwrite S and dP in place, packed two per column: query columns
+// 0-31 into columns 0-15, 32-63 into 32-47.
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -36,13 +40,16 @@ using namespace ptx;
 
 constexpr int BN = 128;   // keys per CTA
 constexpr int BMQ = 64;   // query rows per block
-constexpr int QS = 2;     // query-block pipeline stages
-constexpr int kThreads = 320;
-constexpr int kProdWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMaxQS = 4;
+constexpr int kThreads = 448;
+constexpr int kCompute = 256;  // threads of the P / dS role
+constexpr int kDrainWarp0 = 8;
+constexpr int kProdWarp = 12;
+constexpr int kMmaWarp = 13;
 
 template <int D>
 struct BwdCfg {
+    static constexpr int QS = D == 128 ? 3 : 4;        // query-block pipeline stages
     static constexpr int kKVBytes = BN * D * 2;        // one K or V tile
     static constexpr int kQBytes = BMQ * D * 2;        // one Q or dO block
     static constexpr int kKOff = 0;
@@ -62,11 +69,16 @@ struct BwdCfg {
 
 struct Bars {
     uint64_t kv_full;
-    uint64_t q_full[QS], q_empty[QS];
+    uint64_t q_full[kMaxQS], q_empty[kMaxQS];
     uint64_t s_full, dp_full, ds_full, dk_done, it_done, dq_empty;
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// TMEM column of k-step kk (16 query rows) of packed P / dS: each half of
+// 32 query columns packs its rows into the first 16 of its own 32 columns,
+// so no half overwrites values the other half has yet to read.
+__device__ __forceinline__ constexpr uint32_t pcol(int kk) { return (kk / 2) * 32 + (kk % 2) * 8; }
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -106,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   BwdArgs a, int n_ktiles) {
     using C = BwdCfg<D>;
+    constexpr int QS = C::QS;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -136,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.dp_full, 1);
-        mbar_init(&bar.ds_full, 128);
+        mbar_init(&bar.ds_full, kCompute);
         mbar_init(&bar.dk_done, 1);
         mbar_init(&bar.it_done, 1);
         mbar_init(&bar.dq_empty, 128);
@@ -182,19 +195,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ph = (t / QS) & 1;
                 const int h = hk * g.G + t / nqb;
                 const int i0 = ilo + (t % nqb) * BMQ;
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar.q_empty[st], ph ^ 1, wd, 0x40))) break;
-                // LSE (as log2 units) and delta of the block's rows
-                for (int r = lane; r < BMQ; r += 32) {
-                    const int i = i0 + r;
-                    float lv = 0.f, dv = 0.f;
+                // LSE (in log2 units) and delta of the block's rows, fetched
+                // while the stage is still in use
+                float lv[2], dv[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int i = i0 + lane + 32 * u;
+                    lv[u] = dv[u] = 0.f;
                     if (i < s.Lq) {
                         const int64_t li = lse_index(g, s, b, h, i);
-                        lv = a.lse[li] * kLog2e;
-                        dv = a.delta[li];
+                        lv[u] = a.lse[li] * kLog2e;
+                        dv[u] = a.delta[li];
                     }
-                    s_lse[st * BMQ + r] = lv;
-                    s_delta[st * BMQ + r] = dv;
                 }
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar.q_empty[st], ph ^ 1, wd, 0x40))) break;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    s_lse[st * BMQ + lane + 32 * u] = lv[u];
+                    s_delta[st * BMQ + lane + 32 * u] = dv[u];
+                }
+                __syncwarp();
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bar.q_full[st], 2 * C::kQBytes);
                     for (int c = 0; c < D / 64; ++c) {
@@ -265,13 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dV += P^T dO, dK += dS^T Q  (B operands MN-major: N = head dim)
 #pragma unroll
                 for (int kk = 0; kk < BMQ / 16; ++kk) {
-                    mma_ts(tmem + C::kTmDV, tmem + C::kTmS + (t & 1) * BMQ + kk * 8,
+                    mma_ts(tmem + C::kTmDV, tmem + C::kTmS + (t & 1) * BMQ + pcol(kk),
                            smem_desc_sw128(sdo + kk * 16 * 128, BMQ * 128, 1024), idKV,
                            (t > 0 || kk > 0));
                 }
 #pragma unroll
                 for (int kk = 0; kk < BMQ / 16; ++kk) {
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + kk * 8,
+                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + pcol(kk),
                            smem_desc_sw128(sq + kk * 16 * 128, BMQ * 128, 1024), idKV,
                            (t > 0 || kk > 0));
                 }
@@ -288,106 +308,112 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bar.it_done);
             }
         }
-    } else if (warp < 4) {
+    } else if (warp < 8) {
         // ------------------------------------------ P, dS (thread = key row)
-        const int j = warp * 32 + lane;      // key within the tile
+        const int half = warp / 4;           // query columns [32 half, 32 half + 32)
+        const int c0 = half * 32;
+        const int j = (warp % 4) * 32 + lane;  // key within the tile
         const int key = n0 + j;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
         const float c2 = g.scale_log2;
         uint8_t *dsrow = smem + C::kDSOff + j * 128;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int st = t % QS;
-            const int i0 = ilo + (t % nqb) * BMQ;
+            const int i0 = ilo + (t % nqb) * BMQ + c0;  // first query row of this half
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, t & 1, wd, 0x60));
             if (!ok) break;
             tc_fence_after();
+            uint32_t pr[32];
+            const uint32_t tS = tmem + C::kTmS + (t & 1) * BMQ + lane_off;
+            tmem_ld32(tS + c0, pr);
             // LSE / delta of this stage are in shared memory once q_full completed
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full[st], (t / QS) & 1, wd, 0x61));
             if (!ok) break;
-            uint32_t pr[BMQ];
-            const uint32_t tS = tmem + C::kTmS + (t & 1) * BMQ + lane_off;
-            tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
-            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
-            const float *lse2 = s_lse + st * BMQ;
-            const float *dlt = s_delta + st * BMQ;
-            const bool full = (i0 + BMQ - 1 < s.Lq) && (n0 + BN - 1 < s.Lkv) &&
+            const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse + st * BMQ + c0);
+            const bool full = (i0 + 31 < s.Lq) && (n0 + BN - 1 < s.Lkv) &&
                               (g.wr < 0 || n0 + BN - 1 <= i0 + g.wr) &&
-                              (g.wl < 0 || n0 >= i0 + BMQ - 1 - g.wl);
-            float p[BMQ];
-            if (full) {
+                              (g.wl < 0 || n0 >= i0 + 31 - g.wl);
+            float p[32];
 #pragma unroll
-                for (int c = 0; c < BMQ; ++c) p[c] = ex2(fmaf(__uint_as_float(pr[c]), c2, -lse2[c]));
-            } else {
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 l4 = lse4[q4];
+                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                for (int c = 0; c < BMQ; ++c) {
-                    const int i = i0 + c;
-                    const bool vis = i < s.Lq && visible(i, key, s.Lkv, g.wl, g.wr);
-                    p[c] = vis ? ex2(fmaf(__uint_as_float(pr[c]), c2, -lse2[c])) : 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * q4 + e;
+                    p[c] = ex2(fmaf(__uint_as_float(pr[c]), c2, -lv[e]));
                 }
             }
-            uint32_t pk[BMQ / 2];
+            if (!full) {
 #pragma unroll
-            for (int c = 0; c < BMQ / 2; ++c) pk[c] = pack2<T>(p[2 * c], p[2 * c + 1]);
-            tmem_st32(tS, pk);
+                for (int c = 0; c < 32; ++c) {
+                    const int i = i0 + c;
+                    if (!(i < s.Lq && visible(i, key, s.Lkv, g.wl, g.wr))) p[c] = 0.f;
+                }
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) pk[c] = pack2<T>(p[2 * c], p[2 * c + 1]);
+            tmem_st16(tS + c0, pk);  // packed into the first 16 of this half's columns
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, t & 1, wd, 0x62));
             if (!ok) break;
             tc_fence_after();
             const uint32_t tP = tmem + C::kTmDP + lane_off;
-            tmem_ld32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pr[0]));
-            tmem_ld32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pr[32]));
+            tmem_ld32(tP + c0, pr);
+            const float4 *dl4 = reinterpret_cast<const float4 *>(s_delta + st * BMQ + c0);
 #pragma unroll
-            for (int c = 0; c < BMQ / 2; ++c) {
-                const float d0 = p[2 * c] * (__uint_as_float(pr[2 * c]) - dlt[2 * c]);
-                const float d1 = p[2 * c + 1] * (__uint_as_float(pr[2 * c + 1]) - dlt[2 * c + 1]);
-                pk[c] = pack2<T>(d0, d1);
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 d4 = dl4[q4];
+                const float d0 = p[4 * q4] * (__uint_as_float(pr[4 * q4]) - d4.x);
+                const float d1 = p[4 * q4 + 1] * (__uint_as_float(pr[4 * q4 + 1]) - d4.y);
+                const float d2 = p[4 * q4 + 2] * (__uint_as_float(pr[4 * q4 + 2]) - d4.z);
+                const float d3 = p[4 * q4 + 3] * (__uint_as_float(pr[4 * q4 + 3]) - d4.w);
+                pk[2 * q4] = pack2<T>(d0, d1);
+                pk[2 * q4 + 1] = pack2<T>(d2, d3);
             }
-            tmem_st32(tP, pk);
-            // dS^T row j into the swizzled MN-major tile (8 chunks of 16 bytes)
+            tmem_st16(tP + c0, pk);
+            // dS^T row j, this half's 4 chunks of the swizzled MN-major tile
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                *reinterpret_cast<uint4 *>(dsrow + ((c ^ (j & 7)) * 16)) = v;
+            for (int q = 0; q < 4; ++q) {
+                const int chunk = c0 / 8 + q;
+                uint4 v = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (j & 7)) * 16)) = v;
             }
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar.ds_full);
         }
-        // epilogue: dK (scaled), dV -> global
+        // epilogue: dK (scaled) from warps 0-3, dV from warps 4-7
         if (ok && n_it > 0)
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.it_done, (n_it - 1) & 1, wd, 0x63));
         tc_fence_after();
         const bool valid = j < nkeys;
-        T *dkrow = (T *)a.dk.ptr + (int64_t)b * a.dk.sb + (int64_t)(s.kv0 + key) * a.dk.ss +
-                   (int64_t)hk * a.dk.sh;
-        T *dvrow = (T *)a.dv.ptr + (int64_t)b * a.dv.sb + (int64_t)(s.kv0 + key) * a.dv.ss +
-                   (int64_t)hk * a.dv.sh;
+        const MutView &ov = half == 0 ? a.dk : a.dv;
+        T *dst = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss +
+                 (int64_t)hk * ov.sh;
+        const float mul = half == 0 ? g.scale : 1.f;
+        const uint32_t base = tmem + (half == 0 ? C::kTmDK : C::kTmDV) + lane_off;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            T *dst = which == 0 ? dkrow : dvrow;
-            const float mul = which == 0 ? g.scale : 1.f;
-            const uint32_t base = tmem + (which == 0 ? C::kTmDK : C::kTmDV) + lane_off;
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            if (n_it > 0) {
+                tmem_ld32(base + cc * 32, v);
+            } else {
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t v[32];
-                if (n_it > 0) {
-                    tmem_ld32(base + cc * 32, v);
-                } else {
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+            if (valid) {
+                uint4 pk4[4];
+                uint32_t *pw = reinterpret_cast<uint32_t *>(pk4);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
-                if (valid) {
-                    uint4 pk4[4];
-                    uint32_t *pw = reinterpret_cast<uint32_t *>(pk4);
+                for (int e = 0; e < 16; ++e)
+                    pw[e] = pack2<T>(__uint_as_float(v[2 * e]) * mul,
+                                     __uint_as_float(v[2 * e + 1]) * mul);
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pw[e] = pack2<T>(__uint_as_float(v[2 * e]) * mul,
-                                         __uint_as_float(v[2 * e + 1]) * mul);
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) d4[e] = pk4[e];
-                }
+                for (int e = 0; e < 4; ++e) d4[e] = pk4[e];
             }
         }
     } else {
@@ -398,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int d = wq * 32 + lane;
         const uint32_t tQ = tmem + C::kTmDQ + ((uint32_t)(wq * 32) << 16);
         const bool has = wq * 32 < D;  // D = 64: lanes 64..127 hold zeros
-        const bool leader = threadIdx.x == 128;
+        const bool leader = threadIdx.x == kDrainWarp0 * 32;
         float *sdq = reinterpret_cast<float *>(smem + C::kDQOff);
         const int64_t rows_total = g.thd ? (int64_t)g.Tq : (int64_t)g.B * g.Sq;
         const int64_t row_base = g.thd ? s.q0 : (int64_t)b * g.Sq;
