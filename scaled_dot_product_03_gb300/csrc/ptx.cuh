@@ -224,6 +224,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Descriptor of the same layout starting `bytes` further on (the start
+// address field holds address >> 4 and never carries out for shared memory).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+    return desc + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation.
 // ab_bf16: 1 for bf16 operands, 0 for fp16.  a_mn / b_mn: 1 when the operand
 // is stored MN-major (transposed), 0 when K-major.

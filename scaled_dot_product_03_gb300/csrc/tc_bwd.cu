@@ -240,16 +240,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K^T as an MN-major operand: atoms of 64 head dims, the second one
             // is the zero tile when D = 64
             constexpr uint32_t kLboKT = D == 128 ? BN * 128 : C::kZeroOff - C::kKOff;
+            // Descriptors are formed once (per stage); each MMA adds a
+            // compile-time offset to the start address.
+            const uint64_t dK = smem_desc_sw128(sK, 16, 1024);       // K, K-major
+            const uint64_t dV = smem_desc_sw128(sV, 16, 1024);       // V, K-major
+            const uint64_t dKT = smem_desc_sw128(sK, kLboKT, 1024);  // K^T, MN-major
+            const uint64_t dDS = smem_desc_sw128(sDS, BN * 128, 1024);
+            auto kmaj_off = [](int kk, int rows) { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
             auto issue_s = [&](int t) {
-                const int st = t % QS;
-                const uint32_t sq = sQ + st * C::kQBytes;
+                const uint64_t db = smem_desc_sw128(sQ + (t % QS) * C::kQBytes, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t offa = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                    const uint32_t offb = (kk / 4) * (BMQ * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + C::kTmS + (t & 1) * BMQ, smem_desc_sw128(sK + offa, 16, 1024),
-                           smem_desc_sw128(sq + offb, 16, 1024), idSP, kk > 0);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::kTmS + (t & 1) * BMQ, desc_add(dK, kmaj_off(kk, BN)),
+                           desc_add(db, kmaj_off(kk, BMQ)), idSP, kk > 0);
                 mma_commit(&bar.s_full);
             };
             bool ok = mbar_wait(&bar.kv_full, 0, wd, 0x50);
@@ -261,16 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; ok && t < n_it; ++t) {
                 const int st = t % QS;
                 const uint32_t sq = sQ + st * C::kQBytes, sdo = sDO + st * C::kQBytes;
+                const uint64_t dDOk = smem_desc_sw128(sdo, 16, 1024);         // dO, K-major
+                const uint64_t dDOm = smem_desc_sw128(sdo, BMQ * 128, 1024);  // dO, MN-major
+                const uint64_t dQm = smem_desc_sw128(sq, BMQ * 128, 1024);    // Q, MN-major
                 // dP^T into the dP buffer, free once iteration t-1's dK finished
                 if (t > 0 && !(ok = mbar_wait(&bar.dk_done, (t - 1) & 1, wd, 0x52))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t offa = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-                    const uint32_t offb = (kk / 4) * (BMQ * 128) + (kk % 4) * 32;
-                    mma_ss(tmem + C::kTmDP, smem_desc_sw128(sV + offa, 16, 1024),
-                           smem_desc_sw128(sdo + offb, 16, 1024), idSP, kk > 0);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::kTmDP, desc_add(dV, kmaj_off(kk, BN)),
+                           desc_add(dDOk, kmaj_off(kk, BMQ)), idSP, kk > 0);
                 mma_commit(&bar.dp_full);
                 // S^T of the next block runs while P and dS of this one are made
                 // (its buffer held P of block t-1, whose dV finished before dk_done)
@@ -284,27 +287,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // dV += P^T dO, dK += dS^T Q  (B operands MN-major: N = head dim)
 #pragma unroll
-                for (int kk = 0; kk < BMQ / 16; ++kk) {
+                for (int kk = 0; kk < BMQ / 16; ++kk)
                     mma_ts(tmem + C::kTmDV, tmem + C::kTmS + (t & 1) * BMQ + pcol(kk),
-                           smem_desc_sw128(sdo + kk * 16 * 128, BMQ * 128, 1024), idKV,
-                           (t > 0 || kk > 0));
-                }
+                           desc_add(dDOm, kk * 16 * 128), idKV, (t > 0 || kk > 0));
 #pragma unroll
-                for (int kk = 0; kk < BMQ / 16; ++kk) {
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + pcol(kk),
-                           smem_desc_sw128(sq + kk * 16 * 128, BMQ * 128, 1024), idKV,
-                           (t > 0 || kk > 0));
-                }
+                for (int kk = 0; kk < BMQ / 16; ++kk)
+                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + pcol(kk), desc_add(dQm, kk * 16 * 128),
+                           idKV, (t > 0 || kk > 0));
                 mma_commit(&bar.q_empty[st]);
                 mma_commit(&bar.dk_done);
                 // dQ^T = K^T dS^T into the dQ buffer, free once drained
                 if (t > 0 && !(ok = mbar_wait(&bar.dq_empty, (t - 1) & 1, wd, 0x54))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    mma_ss(tmem + C::kTmDQ, smem_desc_sw128(sK + kk * 16 * 128, kLboKT, 1024),
-                           smem_desc_sw128(sDS + kk * 16 * 128, BN * 128, 1024), idQ, kk > 0);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ss(tmem + C::kTmDQ, desc_add(dKT, kk * 16 * 128), desc_add(dDS, kk * 16 * 128),
+                           idQ, kk > 0);
                 mma_commit(&bar.it_done);
             }
         }

@@ -188,50 +188,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA
+        // Per tile the chain is S -> softmax -> PV; the tiles alternate so one
+        // tile's MMAs run while the other tile's softmax does.  Issue order per
+        // block jb: PV_0(jb), S_0(jb+1), PV_1(jb), S_1(jb+1).  S_i(jb+1) reuses
+        // the TMEM that P_i(jb) occupies; MMAs issued by one thread execute in
+        // issue order, so it is written only after PV_i(jb) has read P.
+        // Descriptors are formed once; each MMA adds a compile-time offset.
         if (lane == 0 && nb > 0) {
             constexpr uint32_t idS = idesc_f16(BM, BN, kBf16, 0, 0);
             constexpr uint32_t idPV = idesc_f16(BM, D, kBf16, 0, 1);
-            bool ok = mbar_wait(&bar.q_full, 0, wd, 0x20);
+            const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024);
+            auto issue_s = [&](int i, int jb) {  // S_i = Q_i K_jb^T
+                const int st = jb % KS;
+                const uint64_t da = desc_add(dQ, i * C::kTileBytes);
+                const uint64_t db = smem_desc_sw128(sK + st * C::kTileBytes, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    constexpr int kRow = BM * 128;
+                    const uint32_t off = (kk / 4) * kRow + (kk % 4) * 32;
+                    mma_ss(tmem + i * BN, desc_add(da, off), desc_add(db, off), idS, kk > 0);
+                }
+                mma_commit(&bar.s_full[i]);
+            };
+            auto in_range = [&](int i, int jb) { return jb >= tr[i].blo && jb < tr[i].bhi; };
+            bool ok = mbar_wait(&bar.q_full, 0, wd, 0x20) && mbar_wait(&bar.k_full[0], 0, wd, 0x21);
+            if (ok) {
+                tc_fence_after();
+                for (int i = 0; i < NQ; ++i)
+                    if (in_range(i, 0)) issue_s(i, 0);
+                mma_commit(&bar.k_empty[0]);
+            }
             for (int jb = 0; ok && jb < nb; ++jb) {
                 const int st = jb % KS;
                 const uint32_t ph = (jb / KS) & 1;
-                if (!(ok = mbar_wait(&bar.k_full[st], ph, wd, 0x21))) break;
-                tc_fence_after();
-                for (int i = 0; i < NQ; ++i) {
-                    if (jb < tr[i].blo || jb >= tr[i].bhi) continue;
-                    const int t = jb - tr[i].blo;
-                    // S_i still holds P of the previous block until that PV is done
-                    if (t > 0 && !(ok = mbar_wait(&bar.pv_done[i], (t - 1) & 1, wd, 0x22))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                        const uint64_t da = smem_desc_sw128(sQ + i * C::kTileBytes + off, 16, 1024);
-                        const uint64_t db = smem_desc_sw128(sK + st * C::kTileBytes + off, 16, 1024);
-                        mma_ss(tmem + i * BN, da, db, idS, kk > 0);
-                    }
-                    mma_commit(&bar.s_full[i]);
-                }
-                if (!ok) break;
-                mma_commit(&bar.k_empty[st]);
+                const bool has_next = jb + 1 < nb;
                 if (!(ok = mbar_wait(&bar.v_full[st], ph, wd, 0x23))) break;
+                if (has_next &&
+                    !(ok = mbar_wait(&bar.k_full[(jb + 1) % KS], ((jb + 1) / KS) & 1, wd, 0x22)))
+                    break;
                 tc_fence_after();
+                const uint64_t dv = smem_desc_sw128(sV + st * C::kTileBytes, BN * 128, 1024);
                 for (int i = 0; i < NQ; ++i) {
-                    if (jb < tr[i].blo || jb >= tr[i].bhi) continue;
-                    const int t = jb - tr[i].blo;
-                    if (!(ok = mbar_wait(&bar.p_full[i], t & 1, wd, 0x24))) break;
-                    tc_fence_after();
+                    if (in_range(i, jb)) {
+                        const int t = jb - tr[i].blo;
+                        if (!(ok = mbar_wait(&bar.p_full[i], t & 1, wd, 0x24))) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t db = smem_desc_sw128(sV + st * C::kTileBytes + kk * 16 * 128,
-                                                            BN * 128, 1024);
-                        mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8, db, idPV,
-                               (t > 0 || kk > 0));
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8,
+                                   desc_add(dv, kk * 16 * 128), idPV, (t > 0 || kk > 0));
+                        mma_commit(&bar.pv_done[i]);
                     }
-                    mma_commit(&bar.pv_done[i]);
+                    if (has_next && in_range(i, jb + 1)) issue_s(i, jb + 1);
                 }
                 if (!ok) break;
                 mma_commit(&bar.v_empty[st]);
+                if (has_next) mma_commit(&bar.k_empty[(jb + 1) % KS]);
             }
         }
     } else {
