@@ -12,8 +12,9 @@
 //   dV  += P^T dO           P^T rounded to the input type, read from TMEM
 //   dK  += dS^T Q           dS^T read from TMEM
 //   dQ^T = K^T dS^T         dS^T also written to shared memory; the result is
-//                           added to an fp32 dq accumulator in global memory
-//                           with fp32 reductions straight from registers
+//                           staged in shared memory and added to an fp32 dq
+//                           accumulator in global memory by one bulk
+//                           reduction per block
 //
 // (dK and dQ are scaled once at the end.)  Warp roles (448 threads): warps
 // 0-7 compute P and dS (thread = key row; warps 0-3 take query columns 0-31,
@@ -57,7 +58,8 @@ struct BwdCfg {
     static constexpr int kDOOff = kQOff + QS * kQBytes;
     static constexpr int kDSOff = kDOOff + QS * kQBytes;     // dS^T [128 keys][64 q]
     static constexpr int kZeroOff = kDSOff + BN * BMQ * 2;   // zero tile (D = 64 only)
-    static constexpr int kStatOff = kZeroOff + (D == 64 ? BN * 128 : 0);
+    static constexpr int kDQOff = kZeroOff + (D == 64 ? BN * 128 : 0);  // fp32 [64 q][D]
+    static constexpr int kStatOff = kDQOff + BMQ * D * 4;
     static constexpr int kBarOff = kStatOff + QS * BMQ * 2 * 4;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;
     // TMEM columns
@@ -94,8 +96,20 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void red_add_f32(float *addr, float v) {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+// global[0 .. bytes) += shared[0 .. bytes) (fp32), as one bulk operation.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                     gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 template <typename T, int D>
@@ -402,12 +416,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------- dQ^T drain (thread = head dim)
-        // dq accumulator layout: [Hq][rows][D] fp32.  Each thread adds its head
-        // dim of the block's rows; a warp's 32 adds cover 128 contiguous bytes.
+        // dq accumulator layout: [Hq][rows][D] fp32, so the block's rows of one
+        // head are contiguous and go out as a single bulk reduction.
         const int wq = warp % 4;
         const int d = wq * 32 + lane;
         const uint32_t tQ = tmem + C::kTmDQ + ((uint32_t)(wq * 32) << 16);
         const bool has = wq * 32 < D;  // D = 64: lanes 64..127 hold zeros
+        const bool leader = threadIdx.x == kDrainWarp0 * 32;
+        float *sdq = reinterpret_cast<float *>(smem + C::kDQOff);
         const int64_t rows_total = g.thd ? (int64_t)g.Tq : (int64_t)g.B * g.Sq;
         const int64_t row_base = g.thd ? s.q0 : (int64_t)b * g.Sq;
         for (int t = 0; t < n_it; ++t) {
@@ -422,14 +438,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(&bar.dq_empty);
+            if (leader) bulk_wait_read0();  // previous block's staging tile was read
+            named_bar_sync(1, 128);
             if (has) {
+#pragma unroll
+                for (int c = 0; c < BMQ; ++c) sdq[c * D + d] = __uint_as_float(v[c]);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (leader) {
                 const int nrow = min(BMQ, s.Lq - i0);
-                float *dst = a.dq_acc + ((int64_t)h * rows_total + row_base + i0) * D + d;
-#pragma unroll 16
-                for (int c = 0; c < BMQ; ++c)
-                    if (c < nrow) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c]));
+                float *dst = a.dq_acc + ((int64_t)h * rows_total + row_base + i0) * D;
+                bulk_reduce_add_f32(dst, sdq, (uint32_t)(nrow * D * 4));
+                bulk_commit();
             }
         }
+        if (leader) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
