@@ -128,7 +128,7 @@ GBATTN_API attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor
 
 /*
  * Bytes of device scratch memory attn_bwd needs for these parameters
- * (fp32 row terms D_i = <dO_i, O_i> and an fp32 dq accumulator).
+ * (the fp32 row terms delta_i = <dO_i, O_i>, one per query row and head).
  * Returns 0 for invalid parameters.
  */
 GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
@@ -142,7 +142,9 @@ GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
  * sum over the Hq / Hkv query heads that share a key/value head.
  * o and lse must be the forward's outputs for the same inputs.  dq has q's
  * shape, dk and dv k's shape, each with its own strides (they may be views
- * of one packed gradient buffer).  workspace: device memory of at least
+ * of one packed gradient buffer).  Every output element is written by exactly
+ * one thread of one kernel, so results do not depend on scheduling (the
+ * backward is deterministic).  workspace: device memory of at least
  * attn_bwd_workspace_size(p) bytes, 256-byte aligned, whose contents on
  * entry do not matter; it must not be shared with a call that may run at
  * the same time.

@@ -160,16 +160,14 @@ int64_t q_rows(const attn_params *p) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-    size_t delta_off, dq_off, total;
+    size_t delta_off, total;
 };
 
+// Workspace: the fp32 row terms delta_i = <dO_i, O_i>, laid out like LSE.
 WsLayout ws_layout(const attn_params *p) {
     WsLayout w;
-    const size_t rows = (size_t)q_rows(p);
     w.delta_off = 0;
-    w.dq_off = round_up(sizeof(float) * rows * p->Hq, 256);
-    const bool need_acc = uses_tc_bwd(p->dtype, p->D);
-    w.total = w.dq_off + (need_acc ? round_up(sizeof(float) * rows * p->Hq * p->D, 256) : 0);
+    w.total = round_up(sizeof(float) * (size_t)q_rows(p) * p->Hq, 256);
     return w;
 }
 
@@ -279,7 +277,7 @@ attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     a.dk = mview_of(p, dk);
     a.dv = mview_of(p, dv);
     a.delta = (float *)((char *)workspace + w.delta_off);
-    a.dq_acc = uses_tc_bwd(p->dtype, p->D) ? (float *)((char *)workspace + w.dq_off) : nullptr;
+    a.dq_acc = nullptr;
     a.watchdog_ns = watchdog_ns();
     if ((st = device_error_word(&a.err))) return st;
     const cudaStream_t s = (cudaStream_t)stream;

@@ -20,7 +20,8 @@ struct BwdArgs {
     const float *lse;
     MutView dq, dk, dv;
     float *delta;         // workspace: row terms <dO_i, O_i>, laid out like LSE
-    float *dq_acc;        // workspace: fp32 dq accumulator [rows][Hq][D]
+    float *dq_acc;        // optional fp32 accumulator [Hq][rows][D] cleared by the
+                          // preprocess kernel (unused by the current kernels: null)
     unsigned *err;
     uint64_t watchdog_ns;
 };

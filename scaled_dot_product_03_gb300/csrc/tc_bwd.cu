@@ -1,32 +1,27 @@
 // tc_bwd.cu -- tcgen05 backward attention for fp16 / bf16 (head dim 64, 128).
 //
-// One CTA owns a tile of 128 keys of one (batch, key/value head).  K and V
-// stay in shared memory while the CTA walks every 64-row query block of every
-// query head of the group that sees any of its keys.  Per block (q rows i,
-// keys j, all fp32 accumulation in tensor memory):
+// Two kernels, each the only writer of its outputs, so nothing is
+// accumulated across CTAs and the result does not depend on scheduling:
 //
-//   S^T  = K Q^T            (keys x queries)
-//   dP^T = V dO^T
-//   P^T  = exp(scale S^T - LSE)       recomputed from the forward's LSE
-//   dS^T = P^T o (dP^T - delta)       delta_i = <dO_i, O_i> (preprocess kernel)
-//   dV  += P^T dO           P^T rounded to the input type, read from TMEM
-//   dK  += dS^T Q           dS^T read from TMEM
-//   dQ^T = K^T dS^T         dS^T also written to shared memory; the result is
-//                           staged in shared memory and added to an fp32 dq
-//                           accumulator in global memory by one bulk
-//                           reduction per block
+// dK/dV kernel: one CTA per 128 keys of a (batch, key/value head).  K and V
+// stay in shared memory while the CTA walks every 128-row query block of
+// every query head of the group that sees its keys (keys j, queries i):
+//   S^T  = K Q^T,  dP^T = V dO^T          (A and B from shared memory)
+//   P^T  = exp(scale S^T - LSE)           recomputed from the forward's LSE
+//   dS^T = P^T o (dP^T - delta)           delta_i = <dO_i, O_i> (preprocess)
+//   dV  += P^T dO,  dK += dS^T Q          (P^T, dS^T read from TMEM)
+// dQ kernel: one CTA per 128 query rows of a (batch, query head).  Q and dO
+// sit in TMEM as MMA operands while the CTA walks the key blocks its rows see:
+//   S = Q K^T,  dP = dO V^T,  P, dS as above (thread = query row),
+//   dQ += dS K                            (dS read from TMEM)
+// dK and dQ are scaled once at the end.
 //
-// (dK and dQ are scaled once at the end.)  Warp roles (448 threads): warps
-// 0-7 compute P and dS (thread = key row; warps 0-3 take query columns 0-31,
-// warps 4-7 columns 32-63) and store dK (0-3) and dV (4-7) at the end; warps
-// 8-11 drain dQ^T from TMEM into the global accumulator (thread = head dim);
-// warp 12 issues the loads (query blocks run QS stages ahead); warp 13
-// allocates TMEM and issues the MMAs.
-//
-// TMEM columns: dK [0, D), dV [D, 2D), S/P double buffer 2 x 64, dP/dS 64,
-// dQ^T 64 (M = 128 rows; for D = 64 the upper 64 rows multiply a zero tile).
-// P and dS overwrite S and dP in place, packed two per column: query columns
-// 0-31 into columns 0-15, 32-63 into 32-47.
+// In both kernels warps 0-7 compute P and dS for one row each (warps 0-3
+// take columns 0-63 of the block, warps 4-7 columns 64-127) and store the
+// results at the end, warp 8 issues TMA loads and warp 9 allocates TMEM and
+// issues the MMAs.  P and dS overwrite S and dP in TMEM, packed two per
+// column: columns 0-63 of the block into TMEM columns 0-31, 64-127 into
+// 64-95, so neither half overwrites values the other half has yet to read.
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -38,47 +33,19 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BN = 128;   // keys per CTA
-constexpr int BMQ = 64;   // query rows per block
-constexpr int kMaxQS = 4;
-constexpr int kThreads = 448;
-constexpr int kCompute = 256;  // threads of the P / dS role
-constexpr int kDrainWarp0 = 8;
-constexpr int kProdWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int BLK = 128;   // rows of every tile: keys (dK/dV) or queries (dQ)
+constexpr int kThreads = 320;
+constexpr int kCompute = 256;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kMaxStages = 3;
 
-template <int D>
-struct BwdCfg {
-    static constexpr int QS = D == 128 ? 3 : 4;        // query-block pipeline stages
-    static constexpr int kKVBytes = BN * D * 2;        // one K or V tile
-    static constexpr int kQBytes = BMQ * D * 2;        // one Q or dO block
-    static constexpr int kKOff = 0;
-    static constexpr int kVOff = kKOff + kKVBytes;
-    static constexpr int kQOff = kVOff + kKVBytes;
-    static constexpr int kDOOff = kQOff + QS * kQBytes;
-    static constexpr int kDSOff = kDOOff + QS * kQBytes;     // dS^T [128 keys][64 q]
-    static constexpr int kZeroOff = kDSOff + BN * BMQ * 2;   // zero tile (D = 64 only)
-    static constexpr int kDQOff = kZeroOff + (D == 64 ? BN * 128 : 0);  // fp32 [64 q][D]
-    static constexpr int kStatOff = kDQOff + BMQ * D * 4;
-    static constexpr int kBarOff = kStatOff + QS * BMQ * 2 * 4;
-    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
-    // TMEM columns
-    static constexpr int kTmDK = 0, kTmDV = D, kTmS = 2 * D, kTmDP = 2 * D + 128,
-                         kTmDQ = 2 * D + 192;
-};
-
-struct Bars {
-    uint64_t kv_full;
-    uint64_t q_full[kMaxQS], q_empty[kMaxQS];
-    uint64_t s_full, dp_full, ds_full, dk_done, it_done, dq_empty;
-    uint32_t tmem_base;
-    int abort_flag;
-};
-
-// TMEM column of k-step kk (16 query rows) of packed P / dS: each half of
-// 32 query columns packs its rows into the first 16 of its own 32 columns,
-// so no half overwrites values the other half has yet to read.
-__device__ __forceinline__ constexpr uint32_t pcol(int kk) { return (kk / 2) * 32 + (kk % 2) * 8; }
+// TMEM column of k-step kk (16 rows of the block) of packed P / dS.
+__device__ __forceinline__ constexpr uint32_t pcol(int kk) { return (kk / 4) * 64 + (kk % 4) * 8; }
+// Byte offset of k-step kk (16 head dims) in a K-major tile of `rows` rows.
+__device__ __forceinline__ constexpr uint32_t kmaj_off(int kk, int rows) {
+    return (kk / 4) * (rows * 128) + (kk % 4) * 32;
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -96,49 +63,69 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// global[0 .. bytes) += shared[0 .. bytes) (fp32), as one bulk operation.
-__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const void *ssrc, uint32_t bytes) {
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                     gdst),
-                 "r"(smem_u32(ssrc)), "r"(bytes)
-                 : "memory");
+// Writes 32 fp32 values (times mul) of one row as the element type.
+template <typename T>
+__device__ __forceinline__ void store_row32(T *dst, const uint32_t (&v)[32], float mul) {
+    uint4 pk[4];
+    uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        pw[e] = pack2<T>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d4[e] = pk[e];
 }
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
+
+// ===================================================================== dK dV
+template <int D>
+struct KVCfg {
+    static constexpr int QS = D == 128 ? 2 : 3;           // query-block stages
+    static constexpr int kTile = BLK * D * 2;             // one 128 x D tile
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKOff + kTile;
+    static constexpr int kQOff = kVOff + kTile;
+    static constexpr int kDOOff = kQOff + QS * kTile;
+    static constexpr int kStatOff = kDOOff + QS * kTile;  // [QS][128] lse2, [QS][128] delta
+    static constexpr int kBarOff = kStatOff + QS * BLK * 2 * 4;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+    static constexpr int kTmDK = 0, kTmDV = D, kTmS = 2 * D, kTmDP = 2 * D + 128;
+};
+
+struct KVBars {
+    uint64_t kv_full;
+    uint64_t q_full[kMaxStages], q_empty[kMaxStages];
+    uint64_t s_full, dp_full, p_full, ds_full, acc_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  BwdArgs a, int n_ktiles) {
-    using C = BwdCfg<D>;
+    tc_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       BwdArgs a) {
+    using C = KVCfg<D>;
     constexpr int QS = C::QS;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    Bars &bar = *reinterpret_cast<Bars *>(smem + C::kBarOff);
-    float *s_lse = reinterpret_cast<float *>(smem + C::kStatOff);      // [QS][64], log2 units
-    float *s_delta = s_lse + QS * BMQ;                                  // [QS][64]
+    KVBars &bar = *reinterpret_cast<KVBars *>(smem + C::kBarOff);
+    float *s_lse = reinterpret_cast<float *>(smem + C::kStatOff);  // log2 units
+    float *s_delta = s_lse + QS * BLK;
     const Geometry &g = a.g;
 
     const int bh = blockIdx.x % (g.Hkv * g.B);
-    const int kt = blockIdx.x / (g.Hkv * g.B);
+    const int kt = blockIdx.x / (g.Hkv * g.B);  // low key tiles see the most queries
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
-    const int n0 = kt * BN;
+    const int n0 = kt * BLK;
     if (n0 >= s.Lkv) return;
-    const int nkeys = min(BN, s.Lkv - n0);
+    const int nkeys = min(BLK, s.Lkv - n0);
 
     int ilo, ihi;
     query_range(n0, n0 + nkeys, s.Lq, g.wl, g.wr, ilo, ihi);
-    const int nqb = (ihi - ilo + BMQ - 1) / BMQ;  // query blocks per head
-    const int n_it = nqb * g.G;                   // iterations
+    const int nqb = (ihi - ilo + BLK - 1) / BLK;  // query blocks per head
+    const int n_it = nqb * g.G;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -149,17 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.dp_full, 1);
+        mbar_init(&bar.p_full, kCompute);
         mbar_init(&bar.ds_full, kCompute);
-        mbar_init(&bar.dk_done, 1);
-        mbar_init(&bar.it_done, 1);
-        mbar_init(&bar.dq_empty, 128);
+        mbar_init(&bar.acc_done, 1);
         bar.abort_flag = 0;
         fence_mbar_init();
-    }
-    if (D == 64) {  // zero tile standing in for head dims 64..127 of K^T
-        uint4 *z = reinterpret_cast<uint4 *>(smem + C::kZeroOff);
-        for (int e = threadIdx.x; e < BN * 128 / 16; e += kThreads) z[e] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&bar.tmem_base, 512);
@@ -182,11 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ loads
         if (n_it > 0) {
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar.kv_full, 2 * C::kKVBytes);
+                mbar_arrive_expect_tx(&bar.kv_full, 2 * C::kTile);
                 for (int c = 0; c < D / 64; ++c) {
-                    tma_load_4d(smem + C::kKOff + c * BN * 128, &tm_k, &bar.kv_full, c * 64,
+                    tma_load_4d(smem + C::kKOff + c * BLK * 128, &tm_k, &bar.kv_full, c * 64,
                                 s.kv0 + n0, hk, cb);
-                    tma_load_4d(smem + C::kVOff + c * BN * 128, &tm_v, &bar.kv_full, c * 64,
+                    tma_load_4d(smem + C::kVOff + c * BLK * 128, &tm_v, &bar.kv_full, c * 64,
                                 s.kv0 + n0, hk, cb);
                 }
             }
@@ -194,12 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = t % QS;
                 const uint32_t ph = (t / QS) & 1;
                 const int h = hk * g.G + t / nqb;
-                const int i0 = ilo + (t % nqb) * BMQ;
-                // LSE (in log2 units) and delta of the block's rows, fetched
-                // while the stage is still in use
-                float lv[2], dv[2];
+                const int i0 = ilo + (t % nqb) * BLK;
+                // LSE (log2 units) and delta of the block's rows, fetched while
+                // the stage is still in use
+                float lv[4], dv[4];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
+                for (int u = 0; u < 4; ++u) {
                     const int i = i0 + lane + 32 * u;
                     lv[u] = dv[u] = 0.f;
                     if (i < s.Lq) {
@@ -210,17 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!__all_sync(0xffffffffu, mbar_wait(&bar.q_empty[st], ph ^ 1, wd, 0x40))) break;
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    s_lse[st * BMQ + lane + 32 * u] = lv[u];
-                    s_delta[st * BMQ + lane + 32 * u] = dv[u];
+                for (int u = 0; u < 4; ++u) {
+                    s_lse[st * BLK + lane + 32 * u] = lv[u];
+                    s_delta[st * BLK + lane + 32 * u] = dv[u];
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&bar.q_full[st], 2 * C::kQBytes);
+                    mbar_arrive_expect_tx(&bar.q_full[st], 2 * C::kTile);
                     for (int c = 0; c < D / 64; ++c) {
-                        tma_load_4d(smem + C::kQOff + st * C::kQBytes + c * BMQ * 128, &tm_q,
+                        tma_load_4d(smem + C::kQOff + st * C::kTile + c * BLK * 128, &tm_q,
                                     &bar.q_full[st], c * 64, s.q0 + i0, h, cb);
-                        tma_load_4d(smem + C::kDOOff + st * C::kQBytes + c * BMQ * 128, &tm_do,
+                        tma_load_4d(smem + C::kDOOff + st * C::kTile + c * BLK * 128, &tm_do,
                                     &bar.q_full[st], c * 64, s.q0 + i0, h, cb);
                     }
                 } else {
@@ -230,167 +211,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA
+        // Per block t: S^T_t, dP^T_t, then dV_t (once P is written), S^T_{t+1}
+        // (its TMEM held P_t, read by dV_t just before: MMAs of one thread
+        // execute in issue order), dK_t (once dS is written), dP^T_{t+1}.
         if (lane == 0 && n_it > 0) {
-            const uint32_t sK = smem_u32(smem + C::kKOff), sV = smem_u32(smem + C::kVOff);
+            constexpr uint32_t idSP = idesc_f16(BLK, BLK, kBf16, 0, 0);  // S^T, dP^T
+            constexpr uint32_t idKV = idesc_f16(BLK, D, kBf16, 0, 1);    // dV, dK
             const uint32_t sQ = smem_u32(smem + C::kQOff), sDO = smem_u32(smem + C::kDOOff);
-            const uint32_t sDS = smem_u32(smem + C::kDSOff);
-            constexpr uint32_t idSP = idesc_f16(128, BMQ, kBf16, 0, 0);   // S^T, dP^T
-            constexpr uint32_t idKV = idesc_f16(128, D, kBf16, 0, 1);     // dV, dK
-            constexpr uint32_t idQ = idesc_f16(128, BMQ, kBf16, 1, 1);    // dQ^T
-            // K^T as an MN-major operand: atoms of 64 head dims, the second one
-            // is the zero tile when D = 64
-            constexpr uint32_t kLboKT = D == 128 ? BN * 128 : C::kZeroOff - C::kKOff;
-            // Descriptors are formed once (per stage); each MMA adds a
-            // compile-time offset to the start address.
-            const uint64_t dK = smem_desc_sw128(sK, 16, 1024);       // K, K-major
-            const uint64_t dV = smem_desc_sw128(sV, 16, 1024);       // V, K-major
-            const uint64_t dKT = smem_desc_sw128(sK, kLboKT, 1024);  // K^T, MN-major
-            const uint64_t dDS = smem_desc_sw128(sDS, BN * 128, 1024);
-            auto kmaj_off = [](int kk, int rows) { return (kk / 4) * (rows * 128) + (kk % 4) * 32; };
+            const uint64_t dK = smem_desc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+            const uint64_t dV = smem_desc_sw128(smem_u32(smem + C::kVOff), 16, 1024);
             auto issue_s = [&](int t) {
-                const uint64_t db = smem_desc_sw128(sQ + (t % QS) * C::kQBytes, 16, 1024);
+                const uint64_t db = smem_desc_sw128(sQ + (t % QS) * C::kTile, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::kTmS + (t & 1) * BMQ, desc_add(dK, kmaj_off(kk, BN)),
-                           desc_add(db, kmaj_off(kk, BMQ)), idSP, kk > 0);
+                    mma_ss(tmem + C::kTmS, desc_add(dK, kmaj_off(kk, BLK)), desc_add(db, kmaj_off(kk, BLK)),
+                           idSP, kk > 0);
                 mma_commit(&bar.s_full);
             };
-            bool ok = mbar_wait(&bar.kv_full, 0, wd, 0x50);
-            if (ok) ok = mbar_wait(&bar.q_full[0], 0, wd, 0x51);
+            auto issue_dp = [&](int t) {
+                const uint64_t db = smem_desc_sw128(sDO + (t % QS) * C::kTile, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + C::kTmDP, desc_add(dV, kmaj_off(kk, BLK)), desc_add(db, kmaj_off(kk, BLK)),
+                           idSP, kk > 0);
+                mma_commit(&bar.dp_full);
+            };
+            bool ok = mbar_wait(&bar.kv_full, 0, wd, 0x50) && mbar_wait(&bar.q_full[0], 0, wd, 0x51);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
+                issue_dp(0);
             }
             for (int t = 0; ok && t < n_it; ++t) {
                 const int st = t % QS;
-                const uint32_t sq = sQ + st * C::kQBytes, sdo = sDO + st * C::kQBytes;
-                const uint64_t dDOk = smem_desc_sw128(sdo, 16, 1024);         // dO, K-major
-                const uint64_t dDOm = smem_desc_sw128(sdo, BMQ * 128, 1024);  // dO, MN-major
-                const uint64_t dQm = smem_desc_sw128(sq, BMQ * 128, 1024);    // Q, MN-major
-                // dP^T into the dP buffer, free once iteration t-1's dK finished
-                if (t > 0 && !(ok = mbar_wait(&bar.dk_done, (t - 1) & 1, wd, 0x52))) break;
+                const bool next = t + 1 < n_it;
+                // B operands as MN-major (N = head dim) views of the Q / dO tiles
+                const uint64_t dOm = smem_desc_sw128(sDO + st * C::kTile, BLK * 128, 1024);
+                const uint64_t dQm = smem_desc_sw128(sQ + st * C::kTile, BLK * 128, 1024);
+                if (!(ok = mbar_wait(&bar.p_full, t & 1, wd, 0x52))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::kTmDP, desc_add(dV, kmaj_off(kk, BN)),
-                           desc_add(dDOk, kmaj_off(kk, BMQ)), idSP, kk > 0);
-                mma_commit(&bar.dp_full);
-                // S^T of the next block runs while P and dS of this one are made
-                // (its buffer held P of block t-1, whose dV finished before dk_done)
-                if (t + 1 < n_it) {
-                    if (!(ok = mbar_wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, wd, 0x55)))
-                        break;
+                for (int kk = 0; kk < BLK / 16; ++kk)
+                    mma_ts(tmem + C::kTmDV, tmem + C::kTmS + pcol(kk), desc_add(dOm, kk * 16 * 128), idKV,
+                           (t > 0 || kk > 0));
+                if (next) {
+                    if (!(ok = mbar_wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, wd, 0x53))) break;
                     tc_fence_after();
                     issue_s(t + 1);
                 }
-                if (!(ok = mbar_wait(&bar.ds_full, t & 1, wd, 0x53))) break;
+                if (!(ok = mbar_wait(&bar.ds_full, t & 1, wd, 0x54))) break;
                 tc_fence_after();
-                // dV += P^T dO, dK += dS^T Q  (B operands MN-major: N = head dim)
 #pragma unroll
-                for (int kk = 0; kk < BMQ / 16; ++kk)
-                    mma_ts(tmem + C::kTmDV, tmem + C::kTmS + (t & 1) * BMQ + pcol(kk),
-                           desc_add(dDOm, kk * 16 * 128), idKV, (t > 0 || kk > 0));
-#pragma unroll
-                for (int kk = 0; kk < BMQ / 16; ++kk)
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + pcol(kk), desc_add(dQm, kk * 16 * 128),
-                           idKV, (t > 0 || kk > 0));
+                for (int kk = 0; kk < BLK / 16; ++kk)
+                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + pcol(kk), desc_add(dQm, kk * 16 * 128), idKV,
+                           (t > 0 || kk > 0));
                 mma_commit(&bar.q_empty[st]);
-                mma_commit(&bar.dk_done);
-                // dQ^T = K^T dS^T into the dQ buffer, free once drained
-                if (t > 0 && !(ok = mbar_wait(&bar.dq_empty, (t - 1) & 1, wd, 0x54))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ss(tmem + C::kTmDQ, desc_add(dKT, kk * 16 * 128), desc_add(dDS, kk * 16 * 128),
-                           idQ, kk > 0);
-                mma_commit(&bar.it_done);
+                if (next) issue_dp(t + 1);
             }
+            if (ok) mma_commit(&bar.acc_done);
         }
-    } else if (warp < 8) {
-        // ------------------------------------------ P, dS (thread = key row)
-        const int half = warp / 4;           // query columns [32 half, 32 half + 32)
-        const int c0 = half * 32;
+    } else {
+        // --------------------------------------- P, dS (thread = key row)
+        const int half = warp / 4;             // query columns [64 half, 64 half + 64)
+        const int c0 = half * 64;
         const int j = (warp % 4) * 32 + lane;  // key within the tile
         const int key = n0 + j;
         const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+        const uint32_t tS = tmem + C::kTmS + c0 + lane_off;
+        const uint32_t tP = tmem + C::kTmDP + c0 + lane_off;
         const float c2 = g.scale_log2;
-        uint8_t *dsrow = smem + C::kDSOff + j * 128;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int st = t % QS;
-            const int i0 = ilo + (t % nqb) * BMQ + c0;  // first query row of this half
+            const int i0 = ilo + (t % nqb) * BLK + c0;  // first query row of this half
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, t & 1, wd, 0x60));
             if (!ok) break;
             tc_fence_after();
-            uint32_t pr[32];
-            const uint32_t tS = tmem + C::kTmS + (t & 1) * BMQ + lane_off;
-            tmem_ld32(tS + c0, pr);
-            // LSE / delta of this stage are in shared memory once q_full completed
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full[st], (t / QS) & 1, wd, 0x61));
-            if (!ok) break;
-            const float4 *lse4 = reinterpret_cast<const float4 *>(s_lse + st * BMQ + c0);
-            const bool full = (i0 + 31 < s.Lq) && (n0 + BN - 1 < s.Lkv) &&
-                              (g.wr < 0 || n0 + BN - 1 <= i0 + g.wr) &&
-                              (g.wl < 0 || n0 >= i0 + 31 - g.wl);
-            float p[32];
+            // (LSE / delta of stage st were written before q_full completed,
+            // which S^T_t itself waited for)
+            const float *lse2 = s_lse + st * BLK + c0;
+            const float *dlt = s_delta + st * BLK + c0;
+            const bool full = (i0 + 63 < s.Lq) && (n0 + BLK - 1 < s.Lkv) &&
+                              (g.wr < 0 || n0 + BLK - 1 <= i0 + g.wr) &&
+                              (g.wl < 0 || n0 >= i0 + 63 - g.wl);
+            float p[64];
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 l4 = lse4[q4];
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t sr[32];
+                tmem_ld32(tS + 32 * h2, sr);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 4 * q4 + e;
-                    p[c] = ex2(fmaf(__uint_as_float(pr[c]), c2, -lv[e]));
-                }
+                for (int c = 0; c < 32; ++c)
+                    p[32 * h2 + c] = ex2(fmaf(__uint_as_float(sr[c]), c2, -lse2[32 * h2 + c]));
             }
             if (!full) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
+                for (int c = 0; c < 64; ++c) {
                     const int i = i0 + c;
                     if (!(i < s.Lq && visible(i, key, s.Lkv, g.wl, g.wr))) p[c] = 0.f;
                 }
             }
-            uint32_t pk[16];
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) pk[c] = pack2<T>(p[2 * c], p[2 * c + 1]);
-            tmem_st16(tS + c0, pk);  // packed into the first 16 of this half's columns
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, t & 1, wd, 0x62));
+            for (int c = 0; c < 32; ++c) pk[c] = pack2<T>(p[2 * c], p[2 * c + 1]);
+            tmem_st32(tS, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar.p_full);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, t & 1, wd, 0x61));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t tP = tmem + C::kTmDP + lane_off;
-            tmem_ld32(tP + c0, pr);
-            const float4 *dl4 = reinterpret_cast<const float4 *>(s_delta + st * BMQ + c0);
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 d4 = dl4[q4];
-                const float d0 = p[4 * q4] * (__uint_as_float(pr[4 * q4]) - d4.x);
-                const float d1 = p[4 * q4 + 1] * (__uint_as_float(pr[4 * q4 + 1]) - d4.y);
-                const float d2 = p[4 * q4 + 2] * (__uint_as_float(pr[4 * q4 + 2]) - d4.z);
-                const float d3 = p[4 * q4 + 3] * (__uint_as_float(pr[4 * q4 + 3]) - d4.w);
-                pk[2 * q4] = pack2<T>(d0, d1);
-                pk[2 * q4 + 1] = pack2<T>(d2, d3);
-            }
-            tmem_st16(tP + c0, pk);
-            // dS^T row j, this half's 4 chunks of the swizzled MN-major tile
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t dr[32];
+                tmem_ld32(tP + 32 * h2, dr);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int chunk = c0 / 8 + q;
-                uint4 v = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                *reinterpret_cast<uint4 *>(dsrow + ((chunk ^ (j & 7)) * 16)) = v;
+                for (int c = 0; c < 16; ++c) {
+                    const int e = 32 * h2 + 2 * c;
+                    pk[16 * h2 + c] = pack2<T>(p[e] * (__uint_as_float(dr[2 * c]) - dlt[e]),
+                                               p[e + 1] * (__uint_as_float(dr[2 * c + 1]) - dlt[e + 1]));
+                }
             }
+            tmem_st32(tP, pk);
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar.ds_full);
         }
         // epilogue: dK (scaled) from warps 0-3, dV from warps 4-7
-        if (ok && n_it > 0)
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar.it_done, (n_it - 1) & 1, wd, 0x63));
+        if (ok && n_it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.acc_done, 0, wd, 0x62));
         tc_fence_after();
-        const bool valid = j < nkeys;
         const MutView &ov = half == 0 ? a.dk : a.dv;
-        T *dst = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss +
-                 (int64_t)hk * ov.sh;
+        T *dst = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss + (int64_t)hk * ov.sh;
         const float mul = half == 0 ? g.scale : 1.f;
         const uint32_t base = tmem + (half == 0 ? C::kTmDK : C::kTmDV) + lane_off;
 #pragma unroll
@@ -402,58 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0u;
             }
-            if (valid) {
-                uint4 pk4[4];
-                uint32_t *pw = reinterpret_cast<uint32_t *>(pk4);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pw[e] = pack2<T>(__uint_as_float(v[2 * e]) * mul,
-                                     __uint_as_float(v[2 * e + 1]) * mul);
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d4[e] = pk4[e];
-            }
+            if (j < nkeys) store_row32<T>(dst + cc * 32, v, mul);
         }
-    } else {
-        // ------------------------------------- dQ^T drain (thread = head dim)
-        // dq accumulator layout: [Hq][rows][D] fp32, so the block's rows of one
-        // head are contiguous and go out as a single bulk reduction.
-        const int wq = warp % 4;
-        const int d = wq * 32 + lane;
-        const uint32_t tQ = tmem + C::kTmDQ + ((uint32_t)(wq * 32) << 16);
-        const bool has = wq * 32 < D;  // D = 64: lanes 64..127 hold zeros
-        const bool leader = threadIdx.x == kDrainWarp0 * 32;
-        float *sdq = reinterpret_cast<float *>(smem + C::kDQOff);
-        const int64_t rows_total = g.thd ? (int64_t)g.Tq : (int64_t)g.B * g.Sq;
-        const int64_t row_base = g.thd ? s.q0 : (int64_t)b * g.Sq;
-        for (int t = 0; t < n_it; ++t) {
-            const int h = hk * g.G + t / nqb;
-            const int i0 = ilo + (t % nqb) * BMQ;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar.it_done, t & 1, wd, 0x70))) break;
-            tc_fence_after();
-            uint32_t v[BMQ];
-            if (has) {
-                tmem_ld32(tQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(tQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-            }
-            tc_fence_before();
-            mbar_arrive(&bar.dq_empty);
-            if (leader) bulk_wait_read0();  // previous block's staging tile was read
-            named_bar_sync(1, 128);
-            if (has) {
-#pragma unroll
-                for (int c = 0; c < BMQ; ++c) sdq[c * D + d] = __uint_as_float(v[c]);
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (leader) {
-                const int nrow = min(BMQ, s.Lq - i0);
-                float *dst = a.dq_acc + ((int64_t)h * rows_total + row_base + i0) * D;
-                bulk_reduce_add_f32(dst, sdq, (uint32_t)(nrow * D * 4));
-                bulk_commit();
-            }
-        }
-        if (leader) bulk_wait0();
     }
     tc_fence_before();
     __syncthreads();
@@ -464,39 +364,269 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// dq = scale * dq_acc ([Hq][rows][D] fp32), converted and written through
-// dq's strides.
-template <typename T>
-__global__ void dq_convert_kernel(BwdArgs a, int rows) {
+// ======================================================================= dQ
+template <int D>
+struct QCfg {
+    static constexpr int KS = D == 128 ? 2 : 3;  // key/value stages
+    static constexpr int kTile = BLK * D * 2;
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKOff + KS * kTile;
+    static constexpr int kBarOff = kVOff + KS * kTile;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+    static constexpr int kTmQ = 0, kTmDO = D / 2, kTmS = D, kTmDP = D + 128, kTmDQ = D + 256;
+};
+
+struct QBars {
+    uint64_t k_full[kMaxStages], k_empty[kMaxStages], v_full[kMaxStages], v_empty[kMaxStages];
+    uint64_t qd_ready, s_full, s_free, dp_full, ds_full, dq_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     BwdArgs a, int n_mtiles) {
+    using C = QCfg<D>;
+    constexpr int KS = C::KS;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    QBars &bar = *reinterpret_cast<QBars *>(smem + C::kBarOff);
     const Geometry &g = a.g;
-    const int D = g.D;
-    const int64_t n = (int64_t)rows * g.Hq * (D / 8);
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int c8 = (int)(e % (D / 8));
-        const int64_t hr = e / (D / 8);  // h * rows + r
-        const int r = (int)(hr % rows);
-        const int h = (int)(hr / rows);
-        int b = 0, row = r;
-        if (!g.thd) {
-            b = r / g.Sq;
-            row = r % g.Sq;
+
+    const int bh = blockIdx.x % (g.Hq * g.B);
+    const int mt = n_mtiles - 1 - (int)(blockIdx.x / (g.Hq * g.B));  // heaviest first
+    const int h = bh % g.Hq, b = bh / g.Hq;
+    const int hk = h / g.G;
+    const SeqInfo s = seq_info(g, b);
+    const int m0 = mt * BLK;
+    if (m0 >= s.Lq) return;
+    const int nrows = min(BLK, s.Lq - m0);
+    int jlo, jhi;
+    key_range(m0, m0 + nrows, s.Lkv, g.wl, g.wr, jlo, jhi);
+    const int nb = (jhi - jlo + BLK - 1) / BLK;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < KS; ++i) {
+            mbar_init(&bar.k_full[i], 1);
+            mbar_init(&bar.k_empty[i], 1);
+            mbar_init(&bar.v_full[i], 1);
+            mbar_init(&bar.v_empty[i], 1);
         }
-        const float4 *src = reinterpret_cast<const float4 *>(a.dq_acc + hr * D + c8 * 8);
-        const float4 x = src[0], y = src[1];
-        uint4 o;
-        o.x = pack2<T>(x.x * g.scale, x.y * g.scale);
-        o.y = pack2<T>(x.z * g.scale, x.w * g.scale);
-        o.z = pack2<T>(y.x * g.scale, y.y * g.scale);
-        o.w = pack2<T>(y.z * g.scale, y.w * g.scale);
-        T *dst = (T *)a.dq.ptr + (int64_t)b * a.dq.sb + (int64_t)row * a.dq.ss + (int64_t)h * a.dq.sh +
-                 c8 * 8;
-        *reinterpret_cast<uint4 *>(dst) = o;
+        mbar_init(&bar.qd_ready, kCompute);
+        mbar_init(&bar.s_full, 1);
+        mbar_init(&bar.s_free, kCompute);
+        mbar_init(&bar.dp_full, 1);
+        mbar_init(&bar.ds_full, kCompute);
+        mbar_init(&bar.dq_done, 1);
+        bar.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bar.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == kProdWarp && lane == 0) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+    const Watchdog wd{a.watchdog_ns, a.err, &bar.abort_flag};
+    const int cb = g.thd ? 0 : b;
+    const int kv_row = s.kv0 + jlo;
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            for (int jb = 0; jb < nb; ++jb) {
+                const int st = jb % KS;
+                const uint32_t ph = (jb / KS) & 1;
+                if (!mbar_wait(&bar.k_empty[st], ph ^ 1, wd, 0x80)) break;
+                mbar_arrive_expect_tx(&bar.k_full[st], C::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(smem + C::kKOff + st * C::kTile + c * BLK * 128, &tm_k, &bar.k_full[st],
+                                c * 64, kv_row + jb * BLK, hk, cb);
+                if (!mbar_wait(&bar.v_empty[st], ph ^ 1, wd, 0x81)) break;
+                mbar_arrive_expect_tx(&bar.v_full[st], C::kTile);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(smem + C::kVOff + st * C::kTile + c * BLK * 128, &tm_v, &bar.v_full[st],
+                                c * 64, kv_row + jb * BLK, hk, cb);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA
+        // Per block j: S_{j+1} as soon as S_j has been read, dQ += dS_j K_j,
+        // then dP_{j+1} (its TMEM held dS_j, read by the dQ MMA just before).
+        if (lane == 0 && nb > 0) {
+            constexpr uint32_t idS = idesc_f16(BLK, BLK, kBf16, 0, 0);  // S, dP: A from TMEM
+            constexpr uint32_t idQ = idesc_f16(BLK, D, kBf16, 0, 1);    // dQ: B = K, MN-major
+            const uint32_t sK = smem_u32(smem + C::kKOff), sV = smem_u32(smem + C::kVOff);
+            auto issue_s = [&](int jb) {
+                const uint64_t db = smem_desc_sw128(sK + (jb % KS) * C::kTile, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ts(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
+                           kk > 0);
+                mma_commit(&bar.s_full);
+            };
+            auto issue_dp = [&](int jb) {
+                const uint64_t db = smem_desc_sw128(sV + (jb % KS) * C::kTile, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ts(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
+                           kk > 0);
+                mma_commit(&bar.dp_full);
+            };
+            bool ok = mbar_wait(&bar.qd_ready, 0, wd, 0x90) && mbar_wait(&bar.k_full[0], 0, wd, 0x91);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                ok = mbar_wait(&bar.v_full[0], 0, wd, 0x92);
+                tc_fence_after();
+                if (ok) issue_dp(0);
+            }
+            for (int jb = 0; ok && jb < nb; ++jb) {
+                const int st = jb % KS;
+                const bool next = jb + 1 < nb;
+                const int st1 = (jb + 1) % KS;
+                const uint32_t ph1 = ((jb + 1) / KS) & 1;
+                if (next) {
+                    if (!(ok = mbar_wait(&bar.k_full[st1], ph1, wd, 0x93))) break;
+                    if (!(ok = mbar_wait(&bar.s_free, jb & 1, wd, 0x94))) break;
+                    tc_fence_after();
+                    issue_s(jb + 1);
+                }
+                if (!(ok = mbar_wait(&bar.ds_full, jb & 1, wd, 0x95))) break;
+                tc_fence_after();
+                const uint64_t dKm = smem_desc_sw128(sK + st * C::kTile, BLK * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BLK / 16; ++kk)
+                    mma_ts(tmem + C::kTmDQ, tmem + C::kTmDP + pcol(kk), desc_add(dKm, kk * 16 * 128), idQ,
+                           (jb > 0 || kk > 0));
+                mma_commit(&bar.k_empty[st]);
+                mma_commit(&bar.v_empty[st]);
+                if (next) {
+                    if (!(ok = mbar_wait(&bar.v_full[st1], ph1, wd, 0x96))) break;
+                    tc_fence_after();
+                    issue_dp(jb + 1);
+                }
+            }
+            if (ok) mma_commit(&bar.dq_done);
+        }
+    } else {
+        // --------------------------------------- P, dS (thread = query row)
+        const int half = warp / 4;             // key columns [64 half, 64 half + 64)
+        const int c0 = half * 64;
+        const int r = (warp % 4) * 32 + lane;  // row within the tile
+        const int row = m0 + r;
+        const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+        // Q (warps 0-3) or dO (warps 4-7) row into TMEM as an MMA operand
+        {
+            const View &src = half == 0 ? a.q : a.dout;
+            const T *p = (const T *)src.ptr + (int64_t)b * src.sb + (int64_t)(s.q0 + row) * src.ss +
+                         (int64_t)h * src.sh;
+            const uint32_t dstc = tmem + (half == 0 ? C::kTmQ : C::kTmDO) + lane_off;
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t v[32];
+                uint4 *v4 = reinterpret_cast<uint4 *>(v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v4[e] = r < nrows ? reinterpret_cast<const uint4 *>(p + cc * 64)[e] : make_uint4(0, 0, 0, 0);
+                tmem_st32(dstc + cc * 32, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar.qd_ready);
+        }
+        float lse2 = 0.f, dlt = 0.f;
+        if (r < nrows) {
+            const int64_t li = lse_index(g, s, b, h, row);
+            lse2 = a.lse[li] * kLog2e;
+            dlt = a.delta[li];
+        }
+        const uint32_t tS = tmem + C::kTmS + c0 + lane_off;
+        const uint32_t tP = tmem + C::kTmDP + c0 + lane_off;
+        const float c2 = g.scale_log2;
+        bool ok = true;
+        for (int jb = 0; jb < nb; ++jb) {
+            const int k0 = jlo + jb * BLK + c0;  // first key of this half
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, jb & 1, wd, 0xa0));
+            if (!ok) break;
+            tc_fence_after();
+            float p[64];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t sr[32];
+                tmem_ld32(tS + 32 * h2, sr);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) p[32 * h2 + c] = __uint_as_float(sr[c]);
+            }
+            tc_fence_before();
+            mbar_arrive(&bar.s_free);
+            const int rlo = m0, rhi = m0 + nrows - 1;
+            const bool full = (k0 + 63 < s.Lkv) && (g.wr < 0 || k0 + 63 <= rlo + g.wr) &&
+                              (g.wl < 0 || k0 >= rhi - g.wl);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], c2, -lse2));
+            if (!full) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (!(row < s.Lq && visible(row, k0 + c, s.Lkv, g.wl, g.wr))) p[c] = 0.f;
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, jb & 1, wd, 0xa1));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t pk[32];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t dr[32];
+                tmem_ld32(tP + 32 * h2, dr);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const int e = 32 * h2 + 2 * c;
+                    pk[16 * h2 + c] = pack2<T>(p[e] * (__uint_as_float(dr[2 * c]) - dlt),
+                                               p[e + 1] * (__uint_as_float(dr[2 * c + 1]) - dlt));
+                }
+            }
+            tmem_st32(tP, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar.ds_full);
+        }
+        // epilogue: dq = scale * dQ, columns [D/2 half, D/2 half + D/2)
+        if (ok && nb > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.dq_done, 0, wd, 0xa2));
+        tc_fence_after();
+        T *dst = (T *)a.dq.ptr + (int64_t)b * a.dq.sb + (int64_t)(s.q0 + row) * a.dq.ss +
+                 (int64_t)h * a.dq.sh + half * (D / 2);
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t v[32];
+            if (nb > 0) {
+                tmem_ld32(tmem + C::kTmDQ + half * (D / 2) + cc * 32 + lane_off, v);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+            if (r < nrows) store_row32<T>(dst + cc * 32, v, g.scale);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
     }
 }
 
 template <typename T, int D>
-cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, int q_rows, cudaStream_t st) {
+cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
     const uint64_t es = 2;
@@ -515,26 +645,29 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, int q_rows, 
     strides(a.dout, dq, sd);
     CUtensorMap tq, tk, tv, tdo;
     cudaError_t e;
-    if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BMQ)) != cudaSuccess) return e;
-    if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BN)) != cudaSuccess) return e;
-    if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BN)) != cudaSuccess) return e;
-    if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BMQ)) != cudaSuccess) return e;
+    if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BLK)) != cudaSuccess) return e;
+    if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BLK)) != cudaSuccess) return e;
+    if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BLK)) != cudaSuccess) return e;
+    if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BLK)) != cudaSuccess) return e;
     if (max_lkv > 0) {
-        const int smem = BwdCfg<D>::kSmemBytes;
-        auto kern = tc_bwd_kernel<T, D>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-            cudaSuccess)
+        const int smem = KVCfg<D>::kSmemBytes;
+        auto kern = tc_bwd_dkdv_kernel<T, D>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
             return e;
-        const int n_ktiles = (max_lkv + BN - 1) / BN;
-        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
+        const int64_t grid = (int64_t)((max_lkv + BLK - 1) / BLK) * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-        kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a, n_ktiles);
+        kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (q_rows > 0) {
-        const int64_t n = (int64_t)q_rows * g.Hq * (D / 8);
-        const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
-        dq_convert_kernel<T><<<(unsigned)blocks, 256, 0, st>>>(a, q_rows);
+    if (max_lq > 0) {
+        const int smem = QCfg<D>::kSmemBytes;
+        auto kern = tc_bwd_dq_kernel<T, D>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return e;
+        const int n_mtiles = (max_lq + BLK - 1) / BLK;
+        const int64_t grid = (int64_t)n_mtiles * g.Hq * g.B;
+        if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+        kern<<<(unsigned)grid, kThreads, smem, st>>>(tk, tv, a, n_mtiles);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -546,11 +679,12 @@ bool uses_tc_bwd(int dtype, int D) { return (dtype == 0 || dtype == 1) && (D == 
 
 cudaError_t launch_tc_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows,
                           cudaStream_t st) {
+    (void)q_rows;
     switch (dtype * 2 + (a.g.D == 128)) {
-        case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, q_rows, st);
-        case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, q_rows, st);
-        case 2: return launch_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, q_rows, st);
-        case 3: return launch_typed<__nv_bfloat16, 128>(a, max_lq, max_lkv, q_rows, st);
+        case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, st);
+        case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, st);
+        case 2: return launch_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, st);
+        case 3: return launch_typed<__nv_bfloat16, 128>(a, max_lq, max_lkv, st);
     }
     return cudaErrorInvalidValue;
 }
