@@ -46,12 +46,13 @@ def test_noalloc_refuses_problems_larger_than_its_scratch():
     lib = _lib.load()
     p = _lib.AttnParams()
     p.dtype, p.layout = _lib.ATTN_BF16, _lib.ATTN_LAYOUT_DENSE4D
-    p.B, p.Sq, p.Skv, p.Hq, p.Hkv, p.D = 1, 65536, 65536, 4, 4, 128
+    # 64 x 65536 rows x 16 heads of fp32 row terms: 256 MiB of scratch
+    p.B, p.Sq, p.Skv, p.Hq, p.Hkv, p.D = 64, 65536, 65536, 16, 16, 128
     p.scale, p.window_left, p.window_right = 0.125, -1, 0
     assert lib.attn_bwd_workspace_size(ctypes.byref(p)) > _lib.NOALLOC_SCRATCH_BYTES
     t = _lib.AttnTensor()
     t.ptr = 4096
-    t.stride[:] = (65536 * 512, 512, 128, 1)
+    t.stride[:] = (65536 * 2048, 2048, 128, 1)
     st = lib.attn_bwd_noalloc(ctypes.byref(p), t, t, t, t, t, 4096, t, t, t, None)
     assert st == _lib.ATTN_ERR_UNSUPPORTED
     assert b"scratch" in lib.attn_last_error_string()
