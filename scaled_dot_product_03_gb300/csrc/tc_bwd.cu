@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ======================================================================= dQ
 template <int D>
 struct QCfg {
-    static constexpr int KS = D == 128 ? 2 : 3;  // key/value stages
+    static constexpr int KS = 3;  // key/value stages
     static constexpr int kTile = BLK * D * 2;
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + KS * kTile;
