@@ -22,6 +22,7 @@
 // issues the MMAs.  P and dS overwrite S and dP in TMEM, packed two per
 // column: columns 0-63 of the block into TMEM columns 0-31, 64-127 into
 // 64-95, so neither half overwrites values the other half has yet to read.
+#include <algorithm>
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -383,6 +384,36 @@ struct QBars {
     int abort_flag;
 };
 
+// One unit of dQ work: 128 query rows of one (batch, query head).  Work
+// index w enumerates (batch, head) fastest and query tiles from the last
+// (most keys under a causal mask) to the first.
+struct QTile {
+    int b, h, m0, nrows, jlo, nb;
+    SeqInfo s;
+};
+
+__device__ __forceinline__ QTile q_tile(const Geometry &g, int w, int n_mtiles) {
+    QTile t;
+    const int bh = w % (g.Hq * g.B);
+    const int mt = n_mtiles - 1 - w / (g.Hq * g.B);
+    t.h = bh % g.Hq;
+    t.b = bh / g.Hq;
+    t.s = seq_info(g, t.b);
+    t.m0 = mt * BLK;
+    t.nrows = max(0, min(BLK, t.s.Lq - t.m0));
+    t.jlo = 0;
+    t.nb = 0;
+    if (t.nrows > 0) {
+        int jhi;
+        key_range(t.m0, t.m0 + t.nrows, t.s.Lkv, g.wl, g.wr, t.jlo, jhi);
+        t.nb = (jhi - t.jlo + BLK - 1) / BLK;
+    }
+    return t;
+}
+
+// Persistent: each CTA walks work items blockIdx.x, blockIdx.x + gridDim.x,
+// ...; barrier phases and pipeline stages carry over from one item to the
+// next, so the next item's loads and MMAs overlap this item's epilogue.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -394,18 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     QBars &bar = *reinterpret_cast<QBars *>(smem + C::kBarOff);
     const Geometry &g = a.g;
-
-    const int bh = blockIdx.x % (g.Hq * g.B);
-    const int mt = n_mtiles - 1 - (int)(blockIdx.x / (g.Hq * g.B));  // heaviest first
-    const int h = bh % g.Hq, b = bh / g.Hq;
-    const int hk = h / g.G;
-    const SeqInfo s = seq_info(g, b);
-    const int m0 = mt * BLK;
-    if (m0 >= s.Lq) return;
-    const int nrows = min(BLK, s.Lq - m0);
-    int jlo, jhi;
-    key_range(m0, m0 + nrows, s.Lkv, g.wl, g.wr, jlo, jhi);
-    const int nb = (jhi - jlo + BLK - 1) / BLK;
+    const int n_work = n_mtiles * g.Hq * g.B;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -437,183 +457,232 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bar.tmem_base;
     const Watchdog wd{a.watchdog_ns, a.err, &bar.abort_flag};
-    const int cb = g.thd ? 0 : b;
-    const int kv_row = s.kv0 + jlo;
 
     if (warp == kProdWarp) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            for (int jb = 0; jb < nb; ++jb) {
-                const int st = jb % KS;
-                const uint32_t ph = (jb / KS) & 1;
-                if (!mbar_wait(&bar.k_empty[st], ph ^ 1, wd, 0x80)) break;
-                mbar_arrive_expect_tx(&bar.k_full[st], C::kTile);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(smem + C::kKOff + st * C::kTile + c * BLK * 128, &tm_k, &bar.k_full[st],
-                                c * 64, kv_row + jb * BLK, hk, cb);
-                if (!mbar_wait(&bar.v_empty[st], ph ^ 1, wd, 0x81)) break;
-                mbar_arrive_expect_tx(&bar.v_full[st], C::kTile);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(smem + C::kVOff + st * C::kTile + c * BLK * 128, &tm_v, &bar.v_full[st],
-                                c * 64, kv_row + jb * BLK, hk, cb);
+            int gb = 0;  // key blocks loaded so far (all items)
+            bool ok = true;
+            for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+                const QTile tl = q_tile(g, w, n_mtiles);
+                const int cb = g.thd ? 0 : tl.b;
+                const int hk = tl.h / g.G;
+                const int kv_row = tl.s.kv0 + tl.jlo;
+                for (int jb = 0; jb < tl.nb; ++jb, ++gb) {
+                    const int st = gb % KS;
+                    const uint32_t ph = (gb / KS) & 1;
+                    if (!(ok = mbar_wait(&bar.k_empty[st], ph ^ 1, wd, 0x80))) break;
+                    mbar_arrive_expect_tx(&bar.k_full[st], C::kTile);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_4d(smem + C::kKOff + st * C::kTile + c * BLK * 128, &tm_k, &bar.k_full[st],
+                                    c * 64, kv_row + jb * BLK, hk, cb);
+                    if (!(ok = mbar_wait(&bar.v_empty[st], ph ^ 1, wd, 0x81))) break;
+                    mbar_arrive_expect_tx(&bar.v_full[st], C::kTile);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_4d(smem + C::kVOff + st * C::kTile + c * BLK * 128, &tm_v, &bar.v_full[st],
+                                    c * 64, kv_row + jb * BLK, hk, cb);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA
-        // Per block j: S_{j+1} as soon as S_j has been read, dQ += dS_j K_j,
-        // then dP_{j+1} (its TMEM held dS_j, read by the dQ MMA just before).
-        if (lane == 0 && nb > 0) {
+        // Per block: S of the next block as soon as this block's S has been
+        // read, dQ += dS K, then dP of the next block (its TMEM held dS, read
+        // by the dQ MMA just before; MMAs of one thread run in issue order).
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_f16(BLK, BLK, kBf16, 0, 0);  // S, dP: A from TMEM
             constexpr uint32_t idQ = idesc_f16(BLK, D, kBf16, 0, 1);    // dQ: B = K, MN-major
             const uint32_t sK = smem_u32(smem + C::kKOff), sV = smem_u32(smem + C::kVOff);
-            auto issue_s = [&](int jb) {
-                const uint64_t db = smem_desc_sw128(sK + (jb % KS) * C::kTile, 16, 1024);
+            auto issue_s = [&](int gbk) {
+                const uint64_t db = smem_desc_sw128(sK + (gbk % KS) * C::kTile, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
                            kk > 0);
                 mma_commit(&bar.s_full);
             };
-            auto issue_dp = [&](int jb) {
-                const uint64_t db = smem_desc_sw128(sV + (jb % KS) * C::kTile, 16, 1024);
+            auto issue_dp = [&](int gbk) {
+                const uint64_t db = smem_desc_sw128(sV + (gbk % KS) * C::kTile, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
                            kk > 0);
                 mma_commit(&bar.dp_full);
             };
-            bool ok = mbar_wait(&bar.qd_ready, 0, wd, 0x90) && mbar_wait(&bar.k_full[0], 0, wd, 0x91);
-            if (ok) {
+            int gb = 0, tn = 0;  // key blocks and non-empty items so far
+            bool ok = true;
+            for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+                const QTile tl = q_tile(g, w, n_mtiles);
+                if (tl.nb == 0) continue;
+                // Q and dO of this item are in TMEM (written after the previous
+                // item's MMAs had all completed)
+                if (!(ok = mbar_wait(&bar.qd_ready, tn & 1, wd, 0x90))) break;
+                if (!(ok = mbar_wait(&bar.k_full[gb % KS], (gb / KS) & 1, wd, 0x91))) break;
                 tc_fence_after();
-                issue_s(0);
-                ok = mbar_wait(&bar.v_full[0], 0, wd, 0x92);
+                issue_s(gb);
+                if (!(ok = mbar_wait(&bar.v_full[gb % KS], (gb / KS) & 1, wd, 0x92))) break;
                 tc_fence_after();
-                if (ok) issue_dp(0);
-            }
-            for (int jb = 0; ok && jb < nb; ++jb) {
-                const int st = jb % KS;
-                const bool next = jb + 1 < nb;
-                const int st1 = (jb + 1) % KS;
-                const uint32_t ph1 = ((jb + 1) / KS) & 1;
-                if (next) {
-                    if (!(ok = mbar_wait(&bar.k_full[st1], ph1, wd, 0x93))) break;
-                    if (!(ok = mbar_wait(&bar.s_free, jb & 1, wd, 0x94))) break;
+                issue_dp(gb);
+                for (int jb = 0; ok && jb < tl.nb; ++jb) {
+                    const int gbk = gb + jb, st = gbk % KS;
+                    const bool next = jb + 1 < tl.nb;
+                    const int st1 = (gbk + 1) % KS;
+                    const uint32_t ph1 = ((gbk + 1) / KS) & 1;
+                    if (next) {
+                        if (!(ok = mbar_wait(&bar.k_full[st1], ph1, wd, 0x93))) break;
+                        if (!(ok = mbar_wait(&bar.s_free, gbk & 1, wd, 0x94))) break;
+                        tc_fence_after();
+                        issue_s(gbk + 1);
+                    }
+                    if (!(ok = mbar_wait(&bar.ds_full, gbk & 1, wd, 0x95))) break;
                     tc_fence_after();
-                    issue_s(jb + 1);
-                }
-                if (!(ok = mbar_wait(&bar.ds_full, jb & 1, wd, 0x95))) break;
-                tc_fence_after();
-                const uint64_t dKm = smem_desc_sw128(sK + st * C::kTile, BLK * 128, 1024);
+                    const uint64_t dKm = smem_desc_sw128(sK + st * C::kTile, BLK * 128, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BLK / 16; ++kk)
-                    mma_ts(tmem + C::kTmDQ, tmem + C::kTmDP + pcol(kk), desc_add(dKm, kk * 16 * 128), idQ,
-                           (jb > 0 || kk > 0));
-                mma_commit(&bar.k_empty[st]);
-                mma_commit(&bar.v_empty[st]);
-                if (next) {
-                    if (!(ok = mbar_wait(&bar.v_full[st1], ph1, wd, 0x96))) break;
-                    tc_fence_after();
-                    issue_dp(jb + 1);
+                    for (int kk = 0; kk < BLK / 16; ++kk)
+                        mma_ts(tmem + C::kTmDQ, tmem + C::kTmDP + pcol(kk), desc_add(dKm, kk * 16 * 128), idQ,
+                               (jb > 0 || kk > 0));
+                    mma_commit(&bar.k_empty[st]);
+                    mma_commit(&bar.v_empty[st]);
+                    if (next) {
+                        if (!(ok = mbar_wait(&bar.v_full[st1], ph1, wd, 0x96))) break;
+                        tc_fence_after();
+                        issue_dp(gbk + 1);
+                    }
                 }
+                if (!ok) break;
+                mma_commit(&bar.dq_done);
+                gb += tl.nb;
+                ++tn;
             }
-            if (ok) mma_commit(&bar.dq_done);
         }
     } else {
         // --------------------------------------- P, dS (thread = query row)
         const int half = warp / 4;             // key columns [64 half, 64 half + 64)
         const int c0 = half * 64;
         const int r = (warp % 4) * 32 + lane;  // row within the tile
-        const int row = m0 + r;
         const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
-        // Q (warps 0-3) or dO (warps 4-7) row into TMEM as an MMA operand
-        {
-            const View &src = half == 0 ? a.q : a.dout;
-            const T *p = (const T *)src.ptr + (int64_t)b * src.sb + (int64_t)(s.q0 + row) * src.ss +
-                         (int64_t)h * src.sh;
-            const uint32_t dstc = tmem + (half == 0 ? C::kTmQ : C::kTmDO) + lane_off;
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t v[32];
-                uint4 *v4 = reinterpret_cast<uint4 *>(v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    v4[e] = r < nrows ? reinterpret_cast<const uint4 *>(p + cc * 64)[e] : make_uint4(0, 0, 0, 0);
-                tmem_st32(dstc + cc * 32, v);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bar.qd_ready);
-        }
-        float lse2 = 0.f, dlt = 0.f;
-        if (r < nrows) {
-            const int64_t li = lse_index(g, s, b, h, row);
-            lse2 = a.lse[li] * kLog2e;
-            dlt = a.delta[li];
-        }
         const uint32_t tS = tmem + C::kTmS + c0 + lane_off;
         const uint32_t tP = tmem + C::kTmDP + c0 + lane_off;
         const float c2 = g.scale_log2;
+        int gb = 0, tn = 0;
         bool ok = true;
-        for (int jb = 0; jb < nb; ++jb) {
-            const int k0 = jlo + jb * BLK + c0;  // first key of this half
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, jb & 1, wd, 0xa0));
-            if (!ok) break;
-            tc_fence_after();
-            float p[64];
+        // dq rows of the previous item, stored after the next item has started
+        uint32_t pend[D / 2];
+        T *pend_dst = nullptr;
+        for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
+            const QTile tl = q_tile(g, w, n_mtiles);
+            if (tl.nrows == 0) continue;
+            const int row = tl.m0 + r;
+            T *dst = (T *)a.dq.ptr + (int64_t)tl.b * a.dq.sb + (int64_t)(tl.s.q0 + row) * a.dq.ss +
+                     (int64_t)tl.h * a.dq.sh + half * (D / 2);
+            if (tl.nb == 0) {  // no key visible to any row: dq = 0
+                if (r < tl.nrows) {
+                    uint32_t z[32];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t sr[32];
-                tmem_ld32(tS + 32 * h2, sr);
+                    for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) p[32 * h2 + c] = __uint_as_float(sr[c]);
-            }
-            tc_fence_before();
-            mbar_arrive(&bar.s_free);
-            const int rlo = m0, rhi = m0 + nrows - 1;
-            const bool full = (k0 + 63 < s.Lkv) && (g.wr < 0 || k0 + 63 <= rlo + g.wr) &&
-                              (g.wl < 0 || k0 >= rhi - g.wl);
-#pragma unroll
-            for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], c2, -lse2));
-            if (!full) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (!(row < s.Lq && visible(row, k0 + c, s.Lkv, g.wl, g.wr))) p[c] = 0.f;
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, jb & 1, wd, 0xa1));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t pk[32];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t dr[32];
-                tmem_ld32(tP + 32 * h2, dr);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int e = 32 * h2 + 2 * c;
-                    pk[16 * h2 + c] = pack2<T>(p[e] * (__uint_as_float(dr[2 * c]) - dlt),
-                                               p[e + 1] * (__uint_as_float(dr[2 * c + 1]) - dlt));
+                    for (int cc = 0; cc < D / 64; ++cc) store_row32<T>(dst + cc * 32, z, 1.f);
                 }
+                continue;
             }
-            tmem_st32(tP, pk);
-            tmem_wait_st();
+            // Q (warps 0-3) or dO (warps 4-7) row into TMEM as an MMA operand
+            {
+                const View &src = half == 0 ? a.q : a.dout;
+                const T *p = (const T *)src.ptr + (int64_t)tl.b * src.sb + (int64_t)(tl.s.q0 + row) * src.ss +
+                             (int64_t)tl.h * src.sh;
+                const uint32_t dstc = tmem + (half == 0 ? C::kTmQ : C::kTmDO) + lane_off;
+#pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    uint32_t v[32];
+                    uint4 *v4 = reinterpret_cast<uint4 *>(v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v4[e] = r < tl.nrows ? reinterpret_cast<const uint4 *>(p + cc * 64)[e]
+                                             : make_uint4(0, 0, 0, 0);
+                    tmem_st32(dstc + cc * 32, v);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bar.qd_ready);
+            }
+            if (pend_dst) {  // previous item's dq, overlapping this item's first MMAs
+#pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc)
+                    store_row32<T>(pend_dst + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&pend[cc * 32]),
+                                   g.scale);
+                pend_dst = nullptr;
+            }
+            float lse2 = 0.f, dlt = 0.f;
+            if (r < tl.nrows) {
+                const int64_t li = lse_index(g, tl.s, tl.b, tl.h, row);
+                lse2 = a.lse[li] * kLog2e;
+                dlt = a.delta[li];
+            }
+            const int rlo = tl.m0, rhi = tl.m0 + tl.nrows - 1;
+            for (int jb = 0; jb < tl.nb; ++jb) {
+                const int gbk = gb + jb;
+                const int k0 = tl.jlo + jb * BLK + c0;  // first key of this half
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, gbk & 1, wd, 0xa0));
+                if (!ok) break;
+                tc_fence_after();
+                float p[64];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t sr[32];
+                    tmem_ld32(tS + 32 * h2, sr);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) p[32 * h2 + c] = __uint_as_float(sr[c]);
+                }
+                tc_fence_before();
+                mbar_arrive(&bar.s_free);
+                const bool full = (k0 + 63 < tl.s.Lkv) && (g.wr < 0 || k0 + 63 <= rlo + g.wr) &&
+                                  (g.wl < 0 || k0 >= rhi - g.wl);
+#pragma unroll
+                for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], c2, -lse2));
+                if (!full) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (!(row < tl.s.Lq && visible(row, k0 + c, tl.s.Lkv, g.wl, g.wr))) p[c] = 0.f;
+                }
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, gbk & 1, wd, 0xa1));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t pk[32];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t dr[32];
+                    tmem_ld32(tP + 32 * h2, dr);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int e = 32 * h2 + 2 * c;
+                        pk[16 * h2 + c] = pack2<T>(p[e] * (__uint_as_float(dr[2 * c]) - dlt),
+                                                   p[e + 1] * (__uint_as_float(dr[2 * c + 1]) - dlt));
+                    }
+                }
+                tmem_st32(tP, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bar.ds_full);
+            }
+            if (!ok) break;
+            // dq of this item: read now (the next item reuses the TMEM), stored
+            // once the next item's Q / dO are on their way
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dq_done, tn & 1, wd, 0xa2));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc)
+                tmem_ld32(tmem + C::kTmDQ + half * (D / 2) + cc * 32 + lane_off,
+                          *reinterpret_cast<uint32_t(*)[32]>(&pend[cc * 32]));
             tc_fence_before();
-            mbar_arrive(&bar.ds_full);
+            pend_dst = r < tl.nrows ? dst : nullptr;
+            gb += tl.nb;
+            ++tn;
         }
-        // epilogue: dq = scale * dQ, columns [D/2 half, D/2 half + D/2)
-        if (ok && nb > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.dq_done, 0, wd, 0xa2));
-        tc_fence_after();
-        T *dst = (T *)a.dq.ptr + (int64_t)b * a.dq.sb + (int64_t)(s.q0 + row) * a.dq.ss +
-                 (int64_t)h * a.dq.sh + half * (D / 2);
+        if (pend_dst) {
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-            uint32_t v[32];
-            if (nb > 0) {
-                tmem_ld32(tmem + C::kTmDQ + half * (D / 2) + cc * 32 + lane_off, v);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0u;
-            }
-            if (r < nrows) store_row32<T>(dst + cc * 32, v, g.scale);
+            for (int cc = 0; cc < D / 64; ++cc)
+                store_row32<T>(pend_dst + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&pend[cc * 32]), g.scale);
         }
     }
     tc_fence_before();
@@ -623,6 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// Number of SMs of the current device (one persistent CTA per SM).
+cudaError_t sm_count(int *n) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
 }
 
 template <typename T, int D>
@@ -665,9 +742,12 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
             return e;
         const int n_mtiles = (max_lq + BLK - 1) / BLK;
-        const int64_t grid = (int64_t)n_mtiles * g.Hq * g.B;
-        if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-        kern<<<(unsigned)grid, kThreads, smem, st>>>(tk, tv, a, n_mtiles);
+        const int64_t n_work = (int64_t)n_mtiles * g.Hq * g.B;
+        if (n_work > 0x7fffffff) return cudaErrorInvalidConfiguration;
+        int sms = 0;
+        if ((e = sm_count(&sms)) != cudaSuccess) return e;
+        const int grid = (int)std::min<int64_t>(n_work, sms);
+        kern<<<grid, kThreads, smem, st>>>(tk, tv, a, n_mtiles);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
