@@ -27,6 +27,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = dict(B=4, S=4096, H=16, D=128, window=(-1, 0))
+# DRAM bytes (read + write) per launch of the dominant kernel on this workload,
+# from an ncu capture of the same command (gpu__time_duration / dram__bytes
+# metrics; see profiles/); None when the kernel changed after the capture.
+TRAFFIC = {}
 METRIC = "attention TFLOP/s fwd+bwd (bf16 causal) and % of GB300 dense BF16 tensor peak"
 
 
@@ -70,7 +74,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -180,12 +184,16 @@ def run_ours(args):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
+    # every kernel launch inside the timed region is bracketed by CUDA events
+    # on its own stream (the library's per-launch timing hook)
+    gb.profile_begin(8 * args.steps)
     with ClockSampler(local) as clk:
         start.record(stream)
         for i in range(args.steps):
             step(evs[i])
         end.record(stream)
         torch.cuda.synchronize()
+    launches = gb.profile_read(8 * args.steps)
     barrier(ws)
     gb.check_device_error()
     ms_total = max_over_ranks(start.elapsed_time(end), ws)
@@ -196,6 +204,22 @@ def run_ours(args):
     tflops = ws * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
     peaks, src = measured_peaks()
     peak_bf16 = peaks.get("bf16_tflops_sustained" if args.steps * ms_step > 2000 else "bf16_tflops")
+    # per-kernel launch statistics; flops each kernel executes and the part of
+    # them that belongs to the algorithm's count (4 + 10 D N_vis per step)
+    exec_flops = {"fwd": 4.0 * D * nvis, "bwd_dkdv": 8.0 * D * nvis, "bwd_dq": 6.0 * D * nvis}
+    alg_flops = {"fwd": 4.0 * D * nvis, "bwd_dkdv": 8.0 * D * nvis, "bwd_dq": 2.0 * D * nvis}
+    kern = {}
+    for name, ms in launches:
+        kern.setdefault(name, []).append(ms)
+    kernels = {}
+    for name, lst in kern.items():
+        m = statistics.mean(lst)
+        kernels[name] = {"launches": len(lst), "mean_ms": round(m, 4),
+                         "share": round(sum(lst) / max(1e-9, sum(sum(v) for v in kern.values())), 4)}
+        if name in exec_flops:
+            kernels[name]["executed_tflops"] = round(exec_flops[name] / (m * 1e-3) / 1e12, 1)
+            kernels[name]["algorithmic_tflops"] = round(alg_flops[name] / (m * 1e-3) / 1e12, 1)
+    dominant = max(kern, key=lambda k: sum(kern[k]))
 
     # ------------------------------------------------------------- end to end
     # through the public API with host buffers: pinned q, k, v, dO copied in,
@@ -234,11 +258,9 @@ def run_ours(args):
         return None
     fwd_mean = statistics.mean(fwd_ms)
     bwd_mean = statistics.mean(bwd_ms)
-    dominant = "bwd" if bwd_mean >= fwd_mean else "fwd"
-    dom_flops = f_bwd if dominant == "bwd" else f_fwd
-    dom_ms = bwd_mean if dominant == "bwd" else fwd_mean
+    dom_ms = kernels[dominant]["mean_ms"]
+    dom_flops = alg_flops.get(dominant, 0.0)
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    launches_per_step = 1 + gb_launches_bwd(q.dtype, D)
     line = {
         "metric": METRIC,
         "value": round(tflops, 2),
@@ -266,23 +288,18 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
                      "peak": peak_bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_bf16, 4),
-                     "traffic": None, "peak_source": src},
+                     "traffic": TRAFFIC.get(dominant), "peak_source": src,
+                     "algorithmic_flops_per_launch": dom_flops},
+        "kernels": kernels,
         "clocks": clk.summary(),
         "e2e": {"value": None if e2e_tflops is None else round(e2e_tflops, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": len(launches),
         "cpu_baseline": cpu,
         "aux": aux,
     }
     return line
-
-
-def gb_launches_bwd(dtype, D):
-    """Kernels one attn_bwd call launches: row-term preprocess plus the main
-    kernel(s)."""
-    from scaled_dot_product_03_gb300 import _lib
-    return 3
 
 
 def aux_lines(gb, inputs, dev, peaks):
@@ -399,8 +416,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-aux", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

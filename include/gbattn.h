@@ -176,6 +176,29 @@ GBATTN_API attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int
                            float *lse_out, attn_stream_t stream);
 
 /*
+ * Per-launch timing, for benchmarks and profilers.  After
+ * attn_profile_begin(n) the calling thread's next (at most n) kernel
+ * launches by this library are each bracketed by two CUDA events recorded
+ * on the launch stream.  attn_profile_read() waits for those events, writes
+ * each launch's duration in milliseconds to ms[i] and its kind (below) to
+ * kind[i] for i < capacity (either array may be NULL), ends the timing and
+ * returns the number of launches recorded (-1 on a CUDA error).  Recording
+ * events adds no work on the GPU beyond the events themselves.
+ */
+enum {
+    ATTN_KERNEL_FWD = 0,            /* tensor-core forward */
+    ATTN_KERNEL_BWD_PREPROCESS = 1, /* row terms delta_i = <dO_i, O_i> */
+    ATTN_KERNEL_BWD_DKDV = 2,       /* tensor-core dK, dV */
+    ATTN_KERNEL_BWD_DQ = 3,         /* tensor-core dQ */
+    ATTN_KERNEL_MERGE = 4,          /* LSE merge */
+    ATTN_KERNEL_SIMT_FWD = 5,       /* fp32 forward */
+    ATTN_KERNEL_SIMT_BWD_DQ = 6,    /* fp32 dQ */
+    ATTN_KERNEL_SIMT_BWD_DKDV = 7   /* fp32 dK, dV */
+};
+GBATTN_API attn_status attn_profile_begin(int max_launches);
+GBATTN_API int attn_profile_read(float *ms, int *kind, int capacity);
+
+/*
  * attn_bwd without a caller-provided workspace.  (The source pages have no
  * counterpart: this entry point exists for callers of the library, not for
  * the method.)

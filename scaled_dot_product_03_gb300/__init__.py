@@ -21,6 +21,7 @@ from . import _lib
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_merge_lse", "attn_bwd_workspace_size",
            "check_device_error", "set_watchdog_ns", "watchdog_selftest", "AttnError",
+           "profile_begin", "profile_read",
            "params_for"]
 
 AttnError = _lib.AttnError
@@ -200,6 +201,24 @@ def attn_merge_lse(o1, lse1, o2, lse2, *, out=None, lse_out=None
                                   lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
                                   _tensor(views[2], False), lse_out.data_ptr(), _stream(o1)))
     return out, lse_out
+
+
+def profile_begin(max_launches: int) -> None:
+    """Start timing each kernel launch of the calling thread (see
+    attn_profile_begin in include/gbattn.h)."""
+    _lib.check(_lib.load().attn_profile_begin(int(max_launches)))
+
+
+def profile_read(capacity: int = 4096):
+    """Stop timing; returns ``[(kind_name, milliseconds), ...]`` per launch."""
+    import ctypes
+    ms = (ctypes.c_float * capacity)()
+    kind = (ctypes.c_int * capacity)()
+    n = _lib.load().attn_profile_read(ctypes.cast(ms, ctypes.c_void_p),
+                                      ctypes.cast(kind, ctypes.c_void_p), capacity)
+    if n < 0:
+        raise AttnError(_lib.ATTN_ERR_CUDA, "attn_profile_read failed")
+    return [(_lib.KERNEL_KINDS.get(kind[i], str(kind[i])), float(ms[i])) for i in range(n)]
 
 
 def check_device_error(device=None) -> None:

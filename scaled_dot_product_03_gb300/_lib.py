@@ -21,7 +21,10 @@ ATTN_LAYOUT_DENSE4D, ATTN_LAYOUT_THD = 0, 1
 # Every symbol include/gbattn.h declares.
 EXPORTS = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_merge_lse",
            "attn_last_error_string", "attn_check_device_error", "attn_set_watchdog_ns",
-           "attn_watchdog_selftest", "attn_bwd_noalloc")
+           "attn_watchdog_selftest", "attn_profile_begin", "attn_profile_read",
+           "attn_bwd_noalloc")
+KERNEL_KINDS = {0: "fwd", 1: "bwd_preprocess", 2: "bwd_dkdv", 3: "bwd_dq", 4: "merge",
+                5: "simt_fwd", 6: "simt_bwd_dq", 7: "simt_bwd_dkdv"}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 
@@ -79,6 +82,10 @@ def load(path: str = LIB_PATH):
         lib.attn_set_watchdog_ns.restype = ctypes.c_uint64
         lib.attn_watchdog_selftest.argtypes = [S]
         lib.attn_watchdog_selftest.restype = i32
+        lib.attn_profile_begin.argtypes = [i32]
+        lib.attn_profile_begin.restype = i32
+        lib.attn_profile_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i32]
+        lib.attn_profile_read.restype = i32
         lib.attn_bwd_noalloc.argtypes = [P, T, T, T, T, T, f32p, T, T, T, S]
         lib.attn_bwd_noalloc.restype = i32
         _lib = lib

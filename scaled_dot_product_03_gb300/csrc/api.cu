@@ -8,7 +8,9 @@
 
 #include "gbattn.h"
 #include "launch.h"
+#include "prof.h"
 #include "tc.h"
+#include <vector>
 
 namespace gbattn {
 namespace {
@@ -173,6 +175,31 @@ WsLayout ws_layout(const attn_params *p) {
 
 }  // namespace
 
+// ----------------------------------------------------------------- timing
+// Per-thread launch timing: while enabled, each kernel launch is bracketed
+// by two events recorded on its stream.
+struct ProfState {
+    bool on = false;
+    int cap = 0, n = 0;
+    std::vector<cudaEvent_t> ev;  // 2 per launch
+    std::vector<int> kind;
+};
+thread_local ProfState t_prof;
+
+void prof_before(cudaStream_t st, int kind) {
+    ProfState &p = t_prof;
+    if (!p.on || p.n >= p.cap) return;
+    cudaEventRecord(p.ev[2 * p.n], st);
+    p.kind[p.n] = kind;
+}
+
+void prof_after(cudaStream_t st) {
+    ProfState &p = t_prof;
+    if (!p.on || p.n >= p.cap) return;
+    cudaEventRecord(p.ev[2 * p.n + 1], st);
+    ++p.n;
+}
+
 attn_status record_error(attn_status st, const char *msg) {
     t_error = msg;
     return st;
@@ -323,6 +350,43 @@ attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int D, attn_te
     cudaError_t e = launch_merge(dtype, a, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "attn_merge_lse launch");
     return ATTN_OK;
+}
+
+attn_status attn_profile_begin(int max_launches) {
+    t_error.clear();
+    if (max_launches < 1) return fail(ATTN_ERR_INVALID_ARG, "max_launches must be positive");
+    ProfState &p = t_prof;
+    if ((int)p.ev.size() < 2 * max_launches) {
+        const size_t old = p.ev.size();
+        p.ev.resize(2 * (size_t)max_launches);
+        for (size_t i = old; i < p.ev.size(); ++i) {
+            cudaError_t e = cudaEventCreate(&p.ev[i]);
+            if (e != cudaSuccess) {
+                p.ev.resize(i);
+                return cuda_fail(e, "cudaEventCreate");
+            }
+        }
+    }
+    p.kind.assign(max_launches, -1);
+    p.cap = max_launches;
+    p.n = 0;
+    p.on = true;
+    return ATTN_OK;
+}
+
+int attn_profile_read(float *ms, int *kind, int capacity) {
+    ProfState &p = t_prof;
+    if (!p.on) return 0;
+    p.on = false;
+    const int n = p.n < capacity ? p.n : capacity;
+    for (int i = 0; i < n; ++i) {
+        if (cudaEventSynchronize(p.ev[2 * i + 1]) != cudaSuccess) return -1;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, p.ev[2 * i], p.ev[2 * i + 1]) != cudaSuccess) return -1;
+        if (ms) ms[i] = t;
+        if (kind) kind[i] = p.kind[i];
+    }
+    return n;
 }
 
 attn_status attn_watchdog_selftest(attn_stream_t stream) {

@@ -10,6 +10,7 @@
 // vectors of the row, so rows never straddle warps and an in-place update of
 // the LSE (lse_out == lse1) is ordered after every lane has read it.
 #include "launch.h"
+#include "prof.h"
 
 namespace gbattn {
 namespace {
@@ -78,7 +79,9 @@ cudaError_t merge_typed(const MergeArgs &a, cudaStream_t st) {
     int64_t blocks = (warps_needed + 7) / 8;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
+    prof_before(st, kProfMerge);
     merge_kernel<T, VEC><<<(int)blocks, 256, 0, st>>>(a, tpr);
+    prof_after(st);
     return cudaGetLastError();
 }
 

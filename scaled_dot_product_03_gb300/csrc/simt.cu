@@ -12,6 +12,7 @@
 // (thread per query row) and one for dk/dv (four threads per key, summing
 // over the query heads of the group), each recomputing P from the saved LSE.
 #include "launch.h"
+#include "prof.h"
 
 namespace gbattn {
 namespace {
@@ -333,7 +334,9 @@ cudaError_t fwd_typed(const FwdArgs &a, int max_lq, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((max_lq + kThreads - 1) / kThreads, a.g.Hq, a.g.B);
+    prof_before(st, kProfSimtFwd);
     k<<<grid, kThreads, smem, st>>>(a);
+    prof_after(st);
     return cudaGetLastError();
 }
 
@@ -345,7 +348,9 @@ cudaError_t bwd_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         dim3 grid((max_lq + kThreads - 1) / kThreads, a.g.Hq, a.g.B);
+        prof_before(st, kProfSimtBwdDq);
         k<<<grid, kThreads, smem, st>>>(a);
+        prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (max_lkv > 0) {
@@ -354,7 +359,9 @@ cudaError_t bwd_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         dim3 grid((max_lkv + kThreads / 4 - 1) / (kThreads / 4), a.g.Hkv, a.g.B);
+        prof_before(st, kProfSimtBwdDkDv);
         k<<<grid, kThreads, smem, st>>>(a);
+        prof_after(st);
         return cudaGetLastError();
     }
     return cudaSuccess;
@@ -387,7 +394,9 @@ void preprocess_typed(const BwdArgs &a, int rows, cudaStream_t st) {
     int64_t blocks = (warps + 7) / 8;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
+    prof_before(st, kProfBwdPreprocess);
     bwd_preprocess_kernel<T, VEC><<<(unsigned)blocks, 256, 0, st>>>(a, rows);
+    prof_after(st);
 }
 }  // namespace
 

@@ -27,6 +27,7 @@
 
 #include "ptx.cuh"
 #include "tc.h"
+#include "prof.h"
 #include "tmap.h"
 
 namespace gbattn {
@@ -733,7 +734,9 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t
             return e;
         const int64_t grid = (int64_t)((max_lkv + BLK - 1) / BLK) * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+        prof_before(st, kProfBwdDkDv);
         kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a);
+        prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (max_lq > 0) {
@@ -747,7 +750,9 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t
         int sms = 0;
         if ((e = sm_count(&sms)) != cudaSuccess) return e;
         const int grid = (int)std::min<int64_t>(n_work, sms);
+        prof_before(st, kProfBwdDq);
         kern<<<grid, kThreads, smem, st>>>(tk, tv, a, n_mtiles);
+        prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

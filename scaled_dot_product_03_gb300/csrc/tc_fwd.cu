@@ -25,6 +25,7 @@
 
 #include "ptx.cuh"
 #include "tc.h"
+#include "prof.h"
 #include "tmap.h"
 
 namespace gbattn {
@@ -395,7 +396,9 @@ cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t
     const int64_t grid = (int64_t)n_mtiles * g.Hq * g.B;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    prof_before(st, kProfFwd);
     kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, a, n_mtiles);
+    prof_after(st);
     return cudaGetLastError();
 }
 
