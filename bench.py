@@ -252,6 +252,8 @@ def run_ours(args):
     e2e_tflops = ws * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12 if e2e_ms == e2e_ms else None
 
     aux = aux_lines(gb, inputs, dev, peaks) if rank == 0 and not args.no_aux else {}
+    if rank == 0 and not args.no_aux:
+        aux["causal_fwd_bwd_sweep"] = sweep_lines(gb, inputs, dev, peaks["bf16_tflops"])
     cpu = cpu_baseline(args) if rank == 0 and ws == 1 and not args.no_cpu else None
 
     if rank != 0:
@@ -300,6 +302,42 @@ def run_ours(args):
         "aux": aux,
     }
     return line
+
+
+def sweep_lines(gb, inputs, dev, peak):
+    """fwd+bwd TFLOP/s of the causal bf16 sequence-length sweep (16384 tokens
+    per batch, H=16, D=128) and of the B=8 S=1024 D=64 case."""
+    import torch
+    res = {}
+    cases = [(16384 // S, S, 16, 128) for S in (1024, 2048, 4096, 8192, 16384)] + [(8, 1024, 16, 64)]
+    for (B, S, H, D) in cases:
+        d = inputs.dense(B, S, H, D, seed=3, dout_seed=4).to(dev)
+        o, lse = gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=(-1, 0))
+        dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+        work = torch.empty(gb.attn_bwd_workspace_size(d.q, d.k, scale=d.scale, window=(-1, 0)),
+                           dtype=torch.uint8, device=dev)
+
+        def one():
+            gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=(-1, 0), out=o, lse=lse)
+            gb.attn_bwd(d.dout, d.q, d.k, d.v, o, lse, scale=d.scale, window=(-1, 0), dq=dq, dk=dk,
+                        dv=dv, workspace=work)
+        for _ in range(3):
+            one()
+        n = 20
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record()
+        for _ in range(n):
+            one()
+        s1.record()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1) / n
+        f_fwd, f_bwd, _ = flops(B, S, H, D, (-1, 0))
+        tf = (f_fwd + f_bwd) / (ms * 1e-3) / 1e12
+        res["B%d_S%d_H%d_D%d" % (B, S, H, D)] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                                 "pct_of_peak": round(100 * tf / peak, 2)}
+        del d, o, lse, dq, dk, dv, work
+    return res
 
 
 def aux_lines(gb, inputs, dev, peaks):

@@ -306,11 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p[32 * h2 + c] = ex2(fmaf(__uint_as_float(sr[c]), c2, -lse2[32 * h2 + c]));
             }
             if (!full) {
+                // queries that see this key: columns [clo, chi) of this half
+                int clo = 0, chi = min(64, s.Lq - i0);
+                if (g.wr >= 0) clo = max(clo, key - g.wr - i0);
+                if (g.wl >= 0) chi = min(chi, key + g.wl + 1 - i0);
+                if (key >= s.Lkv) chi = clo;
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const int i = i0 + c;
-                    if (!(i < s.Lq && visible(i, key, s.Lkv, g.wl, g.wr))) p[c] = 0.f;
-                }
+                for (int c = 0; c < 64; ++c)
+                    if (c < clo || c >= chi) p[c] = 0.f;
             }
             uint32_t pk[32];
 #pragma unroll
@@ -641,9 +644,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(p[c], c2, -lse2));
                 if (!full) {
+                    // keys visible to this row: columns [vlo, vhi) of this half
+                    int vlo = 0, vhi = min(64, tl.s.Lkv - k0);
+                    if (g.wl >= 0) vlo = max(vlo, row - g.wl - k0);
+                    if (g.wr >= 0) vhi = min(vhi, row + g.wr + 1 - k0);
+                    if (row >= tl.s.Lq) vhi = vlo;
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
-                        if (!(row < tl.s.Lq && visible(row, k0 + c, tl.s.Lkv, g.wl, g.wr))) p[c] = 0.f;
+                        if (c < vlo || c >= vhi) p[c] = 0.f;
                 }
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, gbk & 1, wd, 0xa1));
                 if (!ok) break;

@@ -280,9 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
             } else {
+                // keys visible to this row: columns [vlo, vhi) of the block
+                int vlo = 0, vhi = min(BN, s.Lkv - n0);
+                if (g.wl >= 0) vlo = max(vlo, row - g.wl - n0);
+                if (g.wr >= 0) vhi = min(vhi, row + g.wr + 1 - n0);
 #pragma unroll
                 for (int c = 0; c < BN; ++c) {
-                    if (!visible(row, n0 + c, s.Lkv, g.wl, g.wr)) sr[c] = __float_as_uint(-INFINITY);
+                    if (c < vlo || c >= vhi) sr[c] = __float_as_uint(-INFINITY);
                     mx = fmaxf(mx, __uint_as_float(sr[c]));
                 }
             }
