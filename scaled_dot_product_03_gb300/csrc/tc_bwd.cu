@@ -105,7 +105,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       BwdArgs a) {
+                       BwdArgs a, int n_ktiles) {
     using C = KVCfg<D>;
     constexpr int QS = C::QS;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -116,8 +116,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *s_delta = s_lse + QS * BLK;
     const Geometry &g = a.g;
 
-    const int bh = blockIdx.x % (g.Hkv * g.B);
-    const int kt = blockIdx.x / (g.Hkv * g.B);  // low key tiles see the most queries
+    // (batch, head)-major so that the CTAs running at the same time share a
+    // few heads' Q / dO in L2; within a head low key tiles (seen by the most
+    // queries under a causal mask) come first
+    const int bh = blockIdx.x / n_ktiles;
+    const int kt = blockIdx.x % n_ktiles;
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BLK;
@@ -389,8 +392,9 @@ struct QBars {
 };
 
 // One unit of dQ work: 128 query rows of one (batch, query head).  Work
-// index w enumerates (batch, head) fastest and query tiles from the last
-// (most keys under a causal mask) to the first.
+// index w is (batch, head)-major, so the items in flight at the same time
+// share a few heads' K/V in L2, and within a head runs from the last query
+// tile (most keys under a causal mask) to the first.
 struct QTile {
     int b, h, m0, nrows, jlo, nb;
     SeqInfo s;
@@ -398,8 +402,8 @@ struct QTile {
 
 __device__ __forceinline__ QTile q_tile(const Geometry &g, int w, int n_mtiles) {
     QTile t;
-    const int bh = w % (g.Hq * g.B);
-    const int mt = n_mtiles - 1 - w / (g.Hq * g.B);
+    const int bh = w / n_mtiles;
+    const int mt = n_mtiles - 1 - w % n_mtiles;
     t.h = bh % g.Hq;
     t.b = bh / g.Hq;
     t.s = seq_info(g, t.b);
@@ -740,10 +744,11 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t
         auto kern = tc_bwd_dkdv_kernel<T, D>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
             return e;
-        const int64_t grid = (int64_t)((max_lkv + BLK - 1) / BLK) * g.Hkv * g.B;
+        const int n_ktiles = (max_lkv + BLK - 1) / BLK;
+        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdDkDv);
-        kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a);
+        kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
