@@ -84,6 +84,23 @@ __device__ __forceinline__ void query_range(int j0, int j1, int Lq, int wl, int 
     if (hi < lo) hi = lo;
 }
 
+// Work order of the tensor-core kernels.  Work index w covers nt tiles of
+// each of nbh (batch, head) pairs.  Heads are grouped in bands of `band`
+// pairs: the work in flight at one time then touches a few heads' tensors
+// (they stay in L2), and inside a band the tiles go by rank 0 (heaviest)
+// first, each rank across the band's heads, so dispatch stays close to
+// longest-first.
+constexpr int kHeadBand = 8;
+
+__device__ __forceinline__ void banded_order(int w, int nt, int nbh, int &bh, int &rank) {
+    const int per_band = kHeadBand * nt;
+    const int bi = w / per_band, r = w % per_band;
+    const int h0 = bi * kHeadBand;
+    const int bs = min(kHeadBand, nbh - h0);
+    rank = r / bs;
+    bh = h0 + r % bs;
+}
+
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }

@@ -116,11 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *s_delta = s_lse + QS * BLK;
     const Geometry &g = a.g;
 
-    // (batch, head)-major so that the CTAs running at the same time share a
-    // few heads' Q / dO in L2; within a head low key tiles (seen by the most
-    // queries under a causal mask) come first
-    const int bh = blockIdx.x / n_ktiles;
-    const int kt = blockIdx.x % n_ktiles;
+    // banded work order; rank 0 = the first key tiles (seen by the most
+    // queries when causal)
+    int bh, kt;
+    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B, bh, kt);
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BLK;
@@ -391,10 +390,8 @@ struct QBars {
     int abort_flag;
 };
 
-// One unit of dQ work: 128 query rows of one (batch, query head).  Work
-// index w is (batch, head)-major, so the items in flight at the same time
-// share a few heads' K/V in L2, and within a head runs from the last query
-// tile (most keys under a causal mask) to the first.
+// One unit of dQ work: 128 query rows of one (batch, query head), in the
+// banded work order (rank 0 = the last query tile, most keys when causal).
 struct QTile {
     int b, h, m0, nrows, jlo, nb;
     SeqInfo s;
@@ -402,8 +399,9 @@ struct QTile {
 
 __device__ __forceinline__ QTile q_tile(const Geometry &g, int w, int n_mtiles) {
     QTile t;
-    const int bh = w / n_mtiles;
-    const int mt = n_mtiles - 1 - w % n_mtiles;
+    int bh, rank;
+    banded_order(w, n_mtiles, g.Hq * g.B, bh, rank);
+    const int mt = n_mtiles - 1 - rank;
     t.h = bh % g.Hq;
     t.b = bh / g.Hq;
     t.s = seq_info(g, t.b);
@@ -419,9 +417,11 @@ __device__ __forceinline__ QTile q_tile(const Geometry &g, int w, int n_mtiles) 
     return t;
 }
 
-// Persistent: each CTA walks work items blockIdx.x, blockIdx.x + gridDim.x,
-// ...; barrier phases and pipeline stages carry over from one item to the
-// next, so the next item's loads and MMAs overlap this item's epilogue.
+// Each CTA walks work items blockIdx.x, blockIdx.x + gridDim.x, ...; barrier
+// phases and pipeline stages carry over from one item to the next, so with
+// fewer CTAs than items the next item's loads and MMAs overlap this item's
+// epilogue.  The launcher gives one CTA per item, which balances uneven
+// causal items better on this part.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -707,14 +707,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Number of SMs of the current device (one persistent CTA per SM).
-cudaError_t sm_count(int *n) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    return cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
-}
-
 template <typename T, int D>
 cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
@@ -760,9 +752,10 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t
         const int n_mtiles = (max_lq + BLK - 1) / BLK;
         const int64_t n_work = (int64_t)n_mtiles * g.Hq * g.B;
         if (n_work > 0x7fffffff) return cudaErrorInvalidConfiguration;
-        int sms = 0;
-        if ((e = sm_count(&sms)) != cudaSuccess) return e;
-        const int grid = (int)std::min<int64_t>(n_work, sms);
+        // one CTA per work item: the hardware dispatches them in work order as
+        // SMs free up, which balances uneven (causal) items better than a
+        // fixed assignment of items to resident CTAs
+        const int grid = (int)n_work;
         prof_before(st, kProfBwdDq);
         kern<<<grid, kThreads, smem, st>>>(tk, tv, a, n_mtiles);
         prof_after(st);

@@ -96,11 +96,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars &bar = *reinterpret_cast<Bars *>(smem + C::kBarOff);
     const Geometry &g = a.g;
 
-    // (batch, head)-major so that the CTAs running at the same time share a
-    // few heads' K/V in L2; within a head the heaviest tiles (largest row
-    // index under a causal mask) come first
-    const int bh = blockIdx.x / n_mtiles;
-    const int mt = n_mtiles - 1 - (int)(blockIdx.x % n_mtiles);
+    // banded work order; rank 0 = the last query tiles (most keys when causal)
+    int bh, rank;
+    banded_order(blockIdx.x, n_mtiles, g.Hq * g.B, bh, rank);
+    const int mt = n_mtiles - 1 - rank;
     const int h = bh % g.Hq, b = bh / g.Hq;
     const int hk = h / g.G;
     const SeqInfo s = seq_info(g, b);
