@@ -206,8 +206,13 @@ def run_ours(args):
     peak_bf16 = peaks.get("bf16_tflops_sustained" if args.steps * ms_step > 2000 else "bf16_tflops")
     # per-kernel launch statistics; flops each kernel executes and the part of
     # them that belongs to the algorithm's count (4 + 10 D N_vis per step)
-    exec_flops = {"fwd": 4.0 * D * nvis, "bwd_dkdv": 8.0 * D * nvis, "bwd_dq": 6.0 * D * nvis}
-    alg_flops = {"fwd": 4.0 * D * nvis, "bwd_dkdv": 8.0 * D * nvis, "bwd_dq": 2.0 * D * nvis}
+    # (bwd_fused: S, dP, dV, dK and the dQ share, each pair once; the
+    # deterministic two-kernel backward splits them as bwd_dkdv + bwd_dq and
+    # recomputes S and dP in the second)
+    exec_flops = {"fwd": 4.0 * D * nvis, "bwd_fused": 10.0 * D * nvis,
+                  "bwd_dkdv": 8.0 * D * nvis, "bwd_dq": 6.0 * D * nvis}
+    alg_flops = {"fwd": 4.0 * D * nvis, "bwd_fused": 10.0 * D * nvis,
+                 "bwd_dkdv": 8.0 * D * nvis, "bwd_dq": 2.0 * D * nvis}
     kern = {}
     for name, ms in launches:
         kern.setdefault(name, []).append(ms)
@@ -367,6 +372,25 @@ def aux_lines(gb, inputs, dev, peaks):
     out["merge"] = {"workload": "bf16 B=4 S=4096 H=16 D=128", "ms": round(ms, 4),
                     "GB/s": round(gbs, 1), "bound": "hbm", "peak_gbs": peaks["hbm_gbs"],
                     "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes}
+    # the bitwise-reproducible backward (deterministic=True) on the workload
+    wp = inputs.dense(B, S, H, D, window=(-1, 0), seed=7).to(dev)
+    o, lse = gb.attn_fwd(wp.q, wp.k, wp.v, scale=wp.scale, window=(-1, 0))
+    for _ in range(3):
+        gb.attn_bwd(wp.dout, wp.q, wp.k, wp.v, o, lse, scale=wp.scale, window=(-1, 0),
+                    deterministic=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(n):
+        gb.attn_bwd(wp.dout, wp.q, wp.k, wp.v, o, lse, scale=wp.scale, window=(-1, 0),
+                    deterministic=True)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    _, f_bwd, _ = flops(B, S, H, D, (-1, 0))
+    out["bwd_deterministic"] = {"workload": "bf16 causal bwd B=4 S=4096 H=16 D=128, two kernels",
+                                "ms": round(ms, 4),
+                                "TFLOP/s": round(f_bwd / (ms * 1e-3) / 1e12, 1)}
+    del wp, o, lse
     prob = inputs.page3().to(dev)
     for _ in range(3):
         o, lse = gb.attn_fwd(prob.q, prob.k, prob.v, scale=prob.scale)

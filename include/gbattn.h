@@ -114,6 +114,8 @@ typedef struct {
     float scale;         /* softmax scale, finite and > 0, e.g. 1/sqrt(D) */
     int window_left;     /* -1 = unbounded */
     int window_right;    /* -1 = unbounded; (-1, 0) = causal */
+    int deterministic;   /* backward only (see attn_bwd): 0 = single pass with
+                            an fp32 dq accumulator, 1 = bitwise reproducible */
 } attn_params;
 
 /*
@@ -127,9 +129,11 @@ GBATTN_API attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor
                      attn_stream_t stream);
 
 /*
- * Bytes of device scratch memory attn_bwd needs for these parameters
- * (the fp32 row terms delta_i = <dO_i, O_i>, one per query row and head).
- * Returns 0 for invalid parameters.
+ * Bytes of device scratch memory attn_bwd needs for these parameters: the
+ * fp32 row terms delta_i = <dO_i, O_i> (one per query row and head) and,
+ * when the single-pass backward applies (deterministic == 0, fp16 / bf16,
+ * D = 128, at least one query row), an fp32 dq accumulator of D floats per
+ * query row and head.  Returns 0 for invalid parameters.
  */
 GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
 
@@ -142,9 +146,15 @@ GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
  * sum over the Hq / Hkv query heads that share a key/value head.
  * o and lse must be the forward's outputs for the same inputs.  dq has q's
  * shape, dk and dv k's shape, each with its own strides (they may be views
- * of one packed gradient buffer).  Every output element is written by exactly
- * one thread of one kernel, so results do not depend on scheduling (the
- * backward is deterministic).  workspace: device memory of at least
+ * of one packed gradient buffer).
+ * Determinism.  With p->deterministic = 0 and fp16 / bf16 inputs of head
+ * dim 128, one pass over the (key block, query block) pairs forms S and dP
+ * once and adds each pair's share of dq into an fp32 accumulator in the
+ * workspace; those fp32 additions happen in an order set by the GPU's
+ * scheduling, so dq may differ between runs in its last bits (dk and dv do
+ * not).  In every other case (p->deterministic = 1, fp32, D = 64) every
+ * output element is written by exactly one thread of one kernel and the
+ * results do not depend on scheduling.  workspace: device memory of at least
  * attn_bwd_workspace_size(p) bytes, 256-byte aligned, whose contents on
  * entry do not matter; it must not be shared with a call that may run at
  * the same time.
@@ -193,7 +203,9 @@ enum {
     ATTN_KERNEL_MERGE = 4,          /* LSE merge */
     ATTN_KERNEL_SIMT_FWD = 5,       /* fp32 forward */
     ATTN_KERNEL_SIMT_BWD_DQ = 6,    /* fp32 dQ */
-    ATTN_KERNEL_SIMT_BWD_DKDV = 7   /* fp32 dK, dV */
+    ATTN_KERNEL_SIMT_BWD_DKDV = 7,  /* fp32 dK, dV */
+    ATTN_KERNEL_BWD_FUSED = 8,      /* tensor-core single-pass dK, dV, dQ share */
+    ATTN_KERNEL_BWD_DQ_CONVERT = 9  /* fp32 dq accumulator -> dq */
 };
 GBATTN_API attn_status attn_profile_begin(int max_launches);
 GBATTN_API int attn_profile_read(float *ms, int *kind, int capacity);

@@ -55,9 +55,10 @@ def _tensor(t: Optional[torch.Tensor], thd: bool) -> "_lib.AttnTensor":
 
 
 def params_for(q, k, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seqlens_kv=None,
-               max_seqlen_q=None, max_seqlen_kv=None) -> "_lib.AttnParams":
+               max_seqlen_q=None, max_seqlen_kv=None, deterministic=False) -> "_lib.AttnParams":
     """The ``attn_params`` struct describing q (and k, v) views."""
     p = _lib.AttnParams()
+    p.deterministic = 1 if deterministic else 0
     if q.dtype not in _DTYPES:
         raise TypeError("unsupported dtype %s" % q.dtype)
     p.dtype = _DTYPES[q.dtype]
@@ -121,14 +122,18 @@ def attn_bwd_workspace_size(q, k, **kw) -> int:
 
 def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens_q=None,
              cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None, dk=None,
-             dv=None, workspace=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+             dv=None, workspace=None, deterministic=False
+             ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Backward attention: ``(dq, dk, dv)`` for upstream gradient ``dout``,
     recomputing P from q, k and the forward's ``lse``.  ``workspace`` (uint8
-    device tensor of at least :func:`attn_bwd_workspace_size` bytes) is
-    allocated when not given."""
+    device tensor of at least :func:`attn_bwd_workspace_size` bytes, with the
+    same ``deterministic``) is allocated when not given.  ``deterministic``
+    selects the bitwise-reproducible two-kernel backward instead of the
+    single pass whose fp32 dq sums may differ in their last bits between
+    runs."""
     p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
-                   max_seqlen_kv=max_seqlen_kv)
+                   max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
     thd = p.layout == _lib.ATTN_LAYOUT_THD
     lib = _lib.load()
     if dq is None:
@@ -150,7 +155,7 @@ def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens
 
 def attn_bwd_noalloc(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1),
                      cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None,
-                     max_seqlen_kv=None, dq=None, dk=None, dv=None
+                     max_seqlen_kv=None, dq=None, dk=None, dv=None, deterministic=False
                      ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """:func:`attn_bwd` for callers that cannot allocate device scratch: the
     library's own fixed scratch array (``_lib.NOALLOC_SCRATCH_BYTES`` bytes per
@@ -159,7 +164,7 @@ def attn_bwd_noalloc(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1),
     torch allocate dq/dk/dv when they are not passed.)"""
     p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
-                   max_seqlen_kv=max_seqlen_kv)
+                   max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
     thd = p.layout == _lib.ATTN_LAYOUT_THD
     if dq is None:
         dq = torch.empty(q.shape, dtype=q.dtype, device=q.device)

@@ -24,7 +24,8 @@ EXPORTS = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_merge_lse",
            "attn_watchdog_selftest", "attn_profile_begin", "attn_profile_read",
            "attn_bwd_noalloc")
 KERNEL_KINDS = {0: "fwd", 1: "bwd_preprocess", 2: "bwd_dkdv", 3: "bwd_dq", 4: "merge",
-                5: "simt_fwd", 6: "simt_bwd_dq", 7: "simt_bwd_dkdv"}
+                5: "simt_fwd", 6: "simt_bwd_dq", 7: "simt_bwd_dkdv", 8: "bwd_fused",
+                9: "bwd_dq_convert"}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 
@@ -39,7 +40,7 @@ class AttnParams(ctypes.Structure):
                 ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_kv", ctypes.c_void_p),
                 ("max_seqlen_q", ctypes.c_int), ("max_seqlen_kv", ctypes.c_int),
                 ("scale", ctypes.c_float), ("window_left", ctypes.c_int),
-                ("window_right", ctypes.c_int)]
+                ("window_right", ctypes.c_int), ("deterministic", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):

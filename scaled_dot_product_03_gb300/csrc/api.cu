@@ -76,6 +76,8 @@ attn_status check_params(const attn_params *p) {
         return fail(ATTN_ERR_INVALID_ARG, "Hq=%d must be a positive multiple of Hkv=%d", p->Hq, p->Hkv);
     if (p->D != 64 && p->D != 128)
         return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", p->D);
+    if (p->deterministic != 0 && p->deterministic != 1)
+        return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
     if (p->window_left < -1 || p->window_right < -1)
         return fail(ATTN_ERR_INVALID_ARG, "window (%d, %d): each bound must be >= -1",
                     p->window_left, p->window_right);
@@ -161,15 +163,27 @@ int64_t q_rows(const attn_params *p) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Single-pass backward: not asked to be deterministic, covered by the
+// kernel, and at least one query row (the fp32 accumulator is not empty).
+bool fused_bwd(const attn_params *p) {
+    return !p->deterministic && uses_tc_bwd_fused(p->dtype, p->D) && max_lq(p) > 0;
+}
+
 struct WsLayout {
-    size_t delta_off, total;
+    size_t delta_off, acc_off, total;
+    bool fused;
 };
 
-// Workspace: the fp32 row terms delta_i = <dO_i, O_i>, laid out like LSE.
+// Workspace: the fp32 row terms delta_i = <dO_i, O_i>, laid out like LSE,
+// then (single-pass backward only) the fp32 dq accumulator, D floats per
+// LSE entry.
 WsLayout ws_layout(const attn_params *p) {
     WsLayout w;
+    const size_t rows = (size_t)q_rows(p) * p->Hq;
+    w.fused = fused_bwd(p);
     w.delta_off = 0;
-    w.total = round_up(sizeof(float) * (size_t)q_rows(p) * p->Hq, 256);
+    w.acc_off = round_up(sizeof(float) * rows, 256);
+    w.total = w.fused ? w.acc_off + round_up(sizeof(float) * rows * p->D, 256) : w.acc_off;
     return w;
 }
 
@@ -304,13 +318,15 @@ attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     a.dk = mview_of(p, dk);
     a.dv = mview_of(p, dv);
     a.delta = (float *)((char *)workspace + w.delta_off);
-    a.dq_acc = nullptr;
+    a.dq_acc = w.fused ? (float *)((char *)workspace + w.acc_off) : nullptr;
     a.watchdog_ns = watchdog_ns();
     if ((st = device_error_word(&a.err))) return st;
     const cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_bwd_preprocess(p->dtype, a, (int)q_rows(p), s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
-    if (uses_tc_bwd(p->dtype, p->D))
+    if (w.fused)
+        e = launch_tc_bwd_fused(p->dtype, a, max_lkv(p), s);
+    else if (uses_tc_bwd(p->dtype, p->D))
         e = launch_tc_bwd(p->dtype, a, max_lq(p), max_lkv(p), (int)q_rows(p), s);
     else
         e = launch_simt_bwd(p->dtype, a, max_lq(p), max_lkv(p), s);

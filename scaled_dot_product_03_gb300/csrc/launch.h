@@ -20,8 +20,9 @@ struct BwdArgs {
     const float *lse;
     MutView dq, dk, dv;
     float *delta;         // workspace: row terms <dO_i, O_i>, laid out like LSE
-    float *dq_acc;        // optional fp32 accumulator [Hq][rows][D] cleared by the
-                          // preprocess kernel (unused by the current kernels: null)
+    float *dq_acc;        // fp32 dq accumulator laid out like LSE with D columns
+                          // per row, cleared by the preprocess kernel; null when
+                          // the backward does not use one
     unsigned *err;
     uint64_t watchdog_ns;
 };

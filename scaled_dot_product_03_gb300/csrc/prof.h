@@ -17,6 +17,8 @@ enum ProfKind {
     kProfSimtFwd = 5,
     kProfSimtBwdDq = 6,
     kProfSimtBwdDkDv = 7,
+    kProfBwdFused = 8,
+    kProfBwdDqConvert = 9,
 };
 
 void prof_before(cudaStream_t st, int kind);

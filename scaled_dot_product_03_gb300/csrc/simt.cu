@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 // ---------------------------------------------------------------------------
 // Backward preprocess: delta = <dO, O> per (row, head).  A group of up to 32
 // lanes (power of two) covers one (row, head), each lane VEC elements at a
-// time.  Also clears the fp32 dq accumulator ([Hq][rows][D]) when the
-// backward uses one.
+// time.  Also clears the fp32 dq accumulator (laid out like LSE, D floats per
+// row) when the backward uses one.
 template <typename T, int VEC>
 __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
     struct alignas(sizeof(T) * VEC) Vt { T v[VEC]; };
@@ -144,14 +144,20 @@ __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
             }
             const Vt *o = reinterpret_cast<const Vt *>(row_ptr<T>(a.o, b, row, h));
             const Vt *d_o = reinterpret_cast<const Vt *>(row_ptr<T>(a.dout, b, row, h));
-            float *acc_row = a.dq_acc ? a.dq_acc + ((int64_t)h * rows + r) * D : nullptr;
+            float *acc_row = a.dq_acc ? a.dq_acc + idx * D : nullptr;
             for (int c = c0; c < chunks; c += tpr) {
                 const Vt x = o[c], y = d_o[c];
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) acc = fmaf(to_f32(x.v[e]), to_f32(y.v[e]), acc);
                 if (acc_row) {
+                    if (VEC % 4 == 0) {
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc_row[c * VEC + e] = 0.f;
+                        for (int e = 0; e < VEC; e += 4)
+                            *reinterpret_cast<float4 *>(acc_row + c * VEC + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) acc_row[c * VEC + e] = 0.f;
+                    }
                 }
             }
         }

@@ -8,10 +8,15 @@ namespace gbattn {
 // Whether the tensor-core kernels cover this element type and head dim.
 bool uses_tc_fwd(int dtype, int D);
 bool uses_tc_bwd(int dtype, int D);
+// Whether the single-pass backward (fp32 dQ accumulator) covers them.
+bool uses_tc_bwd_fused(int dtype, int D);
 
 cudaError_t launch_tc_fwd(int dtype, const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t st);
 cudaError_t launch_tc_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows,
                           cudaStream_t st);
+// Single-pass backward: needs a.dq_acc (fp32, laid out like LSE with D
+// columns per row) cleared beforehand; writes dk, dv and then dq.
+cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, cudaStream_t st);
 
 // One kernel that waits on an mbarrier nothing arrives on, gives up after
 // `limit_ns`, and records the timeout in *err.

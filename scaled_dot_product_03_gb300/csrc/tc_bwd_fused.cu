@@ -1,0 +1,566 @@
+// tc_bwd_fused.cu -- single-pass tcgen05 backward attention, head dim 128.
+//
+// One CTA per 128 keys of a (batch, key/value head).  K and V stay in shared
+// memory while the CTA walks the 64-row query blocks of every query head of
+// the group that sees its keys; per block (keys j, queries i):
+//   S^T  = K Q^T,  dP^T = V dO^T          (both operands from shared memory)
+//   P^T  = exp(scale S^T - LSE)           recomputed from the forward's LSE
+//   dS^T = P^T o (dP^T - delta)           delta_i = <dO_i, O_i> (preprocess)
+//   dV  += P^T dO                         (P^T from TMEM)
+//   dK  += dS^T Q                         (dS^T from shared memory)
+//   dQ^T = K^T dS^T                       this block's share of dQ
+// S and dP are formed once per (query, key) pair, so the pass executes the
+// five products of the method and nothing more.  dQ sums over every key
+// tile, i.e. over CTAs: each block's share is added into an fp32
+// accumulator in global memory with a TMA bulk reduce-add, and a small
+// kernel scales and converts the sums at the end.  The order of those fp32
+// additions depends on scheduling, so dQ is reproducible only to rounding;
+// dK and dV are owned by one CTA each.
+//
+// Warp roles (448 threads): warps 0-7 compute P and dS (thread = key row;
+// warps 0-3 take query columns 0-31 of the block, warps 4-7 columns 32-63)
+// and write dK / dV at the end; warp 8 issues TMA loads; warp 9 allocates
+// TMEM and issues the MMAs; warps 10-13 drain dQ^T from TMEM (thread = head
+// dim) into shared memory and issue the reductions, warp w owning head dims
+// [32 (w % 4), 32 (w % 4) + 32), which is the TMEM lane quarter it may read.
+//
+// TMEM columns (512): dK 0-127, dV 128-255, S^T / P^T 256-319, dP^T in two
+// buffers 320-383 and 384-447, dQ^T 448-511.  Shared memory: K, V (32 KB
+// each), three stages of Q and dO (16 KB each), two dS^T buffers (16 KB
+// each), the dQ staging boxes (32 KB) and the per-stage LSE / delta.
+#include <type_traits>
+
+#include "ptx.cuh"
+#include "tc.h"
+#include "prof.h"
+#include "tmap.h"
+
+namespace gbattn {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = 128;
+constexpr int BK = 128;   // keys per CTA
+constexpr int BQ = 64;    // query rows per block
+constexpr int QS = 3;     // Q / dO stages
+constexpr int kThreads = 448;
+constexpr int kCompute = 256;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kDrainWarp0 = 10;
+constexpr int kDrain = 128;
+
+constexpr int kKVTile = BK * D * 2;   // 32 KB
+constexpr int kQTile = BQ * D * 2;    // 16 KB
+constexpr int kDSTile = BK * BQ * 2;  // 16 KB
+constexpr int kBox = BQ * 32 * 4;     // 8 KB: 64 rows x 32 fp32
+constexpr int kKOff = 0;
+constexpr int kVOff = kKOff + kKVTile;
+constexpr int kQOff = kVOff + kKVTile;
+constexpr int kDOOff = kQOff + QS * kQTile;
+constexpr int kDSOff = kDOOff + QS * kQTile;
+constexpr int kStgOff = kDSOff + 2 * kDSTile;
+constexpr int kStatOff = kStgOff + 4 * kBox;          // [QS][64] lse2, [QS][64] delta
+constexpr int kBarOff = kStatOff + QS * BQ * 2 * 4;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;      // + barriers + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kTmDK = 0, kTmDV = 128, kTmS = 256, kTmDP = 320, kTmDQ = 448;
+
+struct Bars {
+    uint64_t kv_full;
+    uint64_t q_full[QS], q_empty[QS];
+    uint64_t s_full, p_full;
+    uint64_t dp_full[2], ds_full[2];
+    uint64_t dq_full, dq_free, acc_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// TMEM column of k-step kk (16 query columns) of packed P^T: columns 0-31 of
+// the block are packed into TMEM columns 0-15, 32-63 into 32-47.
+__device__ __forceinline__ constexpr uint32_t pcol(int kk) { return (kk / 2) * 32 + (kk % 2) * 8; }
+// Byte offset of k-step kk (16 head dims) in a K-major tile of `rows` rows.
+__device__ __forceinline__ constexpr uint32_t kmaj_off(int kk, int rows) {
+    return (kk / 4) * (rows * 128) + (kk % 4) * 32;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Adds a 64 x 32 fp32 box from shared memory into the tensor at (x, y, z).
+__device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const CUtensorMap *map, int x, int y, int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            map),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Writes 32 fp32 values (times mul) of one row as the element type.
+template <typename T>
+__device__ __forceinline__ void store_row32(T *dst, const uint32_t (&v)[32], float mul) {
+    uint4 pk[4];
+    uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        pw[e] = pack2<T>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d4[e] = pk[e];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                        const __grid_constant__ CUtensorMap tm_acc, BwdArgs a, int n_ktiles) {
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    Bars &bar = *reinterpret_cast<Bars *>(smem + kBarOff);
+    float *s_lse = reinterpret_cast<float *>(smem + kStatOff);  // log2 units
+    float *s_delta = s_lse + QS * BQ;
+    const Geometry &g = a.g;
+
+    // banded work order; rank 0 = the first key tiles (seen by the most
+    // queries when causal)
+    int bh, kt;
+    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B, bh, kt);
+    const int hk = bh % g.Hkv, b = bh / g.Hkv;
+    const SeqInfo s = seq_info(g, b);
+    const int n0 = kt * BK;
+    if (n0 >= s.Lkv) return;
+    const int nkeys = min(BK, s.Lkv - n0);
+
+    int ilo, ihi;
+    query_range(n0, n0 + nkeys, s.Lq, g.wl, g.wr, ilo, ihi);
+    const int nqb = (ihi - ilo + BQ - 1) / BQ;  // query blocks per head
+    const int n_it = nqb * g.G;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar.kv_full, 1);
+        for (int i = 0; i < QS; ++i) {
+            mbar_init(&bar.q_full[i], 32);
+            mbar_init(&bar.q_empty[i], 1);
+        }
+        mbar_init(&bar.s_full, 1);
+        mbar_init(&bar.p_full, kCompute);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.dp_full[i], 1);
+            mbar_init(&bar.ds_full[i], kCompute);
+        }
+        mbar_init(&bar.dq_full, 1);
+        mbar_init(&bar.dq_free, kDrain);
+        mbar_init(&bar.acc_done, 1);
+        bar.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bar.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == kProdWarp && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_acc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+    const Watchdog wd{a.watchdog_ns, a.err, &bar.abort_flag};
+    const int cb = g.thd ? 0 : b;  // TMA batch coordinate
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------------------ loads
+        if (n_it > 0) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar.kv_full, 2 * kKVTile);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_4d(smem + kKOff + c * BK * 128, &tm_k, &bar.kv_full, c * 64, s.kv0 + n0, hk, cb);
+                    tma_load_4d(smem + kVOff + c * BK * 128, &tm_v, &bar.kv_full, c * 64, s.kv0 + n0, hk, cb);
+                }
+            }
+            for (int t = 0; t < n_it; ++t) {
+                const int st = t % QS;
+                const uint32_t ph = (t / QS) & 1;
+                const int h = hk * g.G + t / nqb;
+                const int i0 = ilo + (t % nqb) * BQ;
+                // LSE (log2 units) and delta of the block's rows, fetched while
+                // the stage is still in use
+                float lv[2], dv[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int i = i0 + lane + 32 * u;
+                    lv[u] = dv[u] = 0.f;
+                    if (i < s.Lq) {
+                        const int64_t li = lse_index(g, s, b, h, i);
+                        lv[u] = a.lse[li] * kLog2e;
+                        dv[u] = a.delta[li];
+                    }
+                }
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar.q_empty[st], ph ^ 1, wd, 0xc0))) break;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    s_lse[st * BQ + lane + 32 * u] = lv[u];
+                    s_delta[st * BQ + lane + 32 * u] = dv[u];
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar.q_full[st], 2 * kQTile);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_4d(smem + kQOff + st * kQTile + c * BQ * 128, &tm_q, &bar.q_full[st], c * 64,
+                                    s.q0 + i0, h, cb);
+                        tma_load_4d(smem + kDOOff + st * kQTile + c * BQ * 128, &tm_do, &bar.q_full[st], c * 64,
+                                    s.q0 + i0, h, cb);
+                    }
+                } else {
+                    mbar_arrive(&bar.q_full[st]);
+                }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA
+        // Per block t: dV_t (once P_t is written), S^T_{t+1} (its TMEM held
+        // P_t, read by dV_t just before: MMAs of one thread execute in issue
+        // order), dP^T_{t+1} (into the other dP buffer), then dK_t and dQ^T_t
+        // once dS_t is in shared memory.
+        if (lane == 0 && n_it > 0) {
+            constexpr uint32_t idSP = idesc_f16(BK, BQ, kBf16, 0, 0);  // S^T, dP^T
+            constexpr uint32_t idKV = idesc_f16(BK, D, kBf16, 0, 1);   // dV, dK: B = dO / Q, MN-major
+            constexpr uint32_t idQ = idesc_f16(D, BQ, kBf16, 1, 1);    // dQ^T: A = K, B = dS^T, MN-major
+            const uint32_t sQ = smem_u32(smem + kQOff), sDO = smem_u32(smem + kDOOff);
+            const uint32_t sDS = smem_u32(smem + kDSOff);
+            const uint64_t dK = smem_desc_sw128(smem_u32(smem + kKOff), 16, 1024);
+            const uint64_t dV = smem_desc_sw128(smem_u32(smem + kVOff), 16, 1024);
+            // K as the MN-major A operand of dQ^T (M = head dim, two 64-wide atoms)
+            const uint64_t dKm = smem_desc_sw128(smem_u32(smem + kKOff), BK * 128, 1024);
+            auto issue_s = [&](int t) {
+                const uint64_t db = smem_desc_sw128(sQ + (t % QS) * kQTile, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + kTmS, desc_add(dK, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
+                mma_commit(&bar.s_full);
+            };
+            auto issue_dp = [&](int t) {
+                const uint64_t db = smem_desc_sw128(sDO + (t % QS) * kQTile, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + kTmDP + (t & 1) * BQ, desc_add(dV, kmaj_off(kk, BK)),
+                           desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
+                mma_commit(&bar.dp_full[t & 1]);
+            };
+            bool ok = mbar_wait(&bar.kv_full, 0, wd, 0xd0) && mbar_wait(&bar.q_full[0], 0, wd, 0xd1);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_dp(0);
+            }
+            for (int t = 0; ok && t < n_it; ++t) {
+                const int st = t % QS;
+                const bool next = t + 1 < n_it;
+                // Q_t / dO_t as MN-major B operands (N = head dim, two 64-wide atoms)
+                const uint64_t dOm = smem_desc_sw128(sDO + st * kQTile, BQ * 128, 1024);
+                const uint64_t dQm = smem_desc_sw128(sQ + st * kQTile, BQ * 128, 1024);
+                if (!(ok = mbar_wait(&bar.p_full, t & 1, wd, 0xd2))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ts(tmem + kTmDV, tmem + kTmS + pcol(kk), desc_add(dOm, kk * 16 * 128), idKV,
+                           (t > 0 || kk > 0));
+                if (next) {
+                    if (!(ok = mbar_wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, wd, 0xd3))) break;
+                    tc_fence_after();
+                    issue_s(t + 1);
+                    issue_dp(t + 1);
+                }
+                if (!(ok = mbar_wait(&bar.ds_full[t & 1], (t >> 1) & 1, wd, 0xd4))) break;
+                tc_fence_after();
+                // dS^T_t: K-major A of dK (K = queries), MN-major B of dQ^T (N = queries)
+                const uint32_t sds = sDS + (t & 1) * kDSTile;
+                const uint64_t dS = smem_desc_sw128(sds, 16, 1024);
+                const uint64_t dSm = smem_desc_sw128(sds, BK * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ss(tmem + kTmDK, desc_add(dS, kk * 32), desc_add(dQm, kk * 16 * 128), idKV,
+                           (t > 0 || kk > 0));
+                mma_commit(&bar.q_empty[st]);
+                if (t > 0 && !(ok = mbar_wait(&bar.dq_free, (t - 1) & 1, wd, 0xd5))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_ss(tmem + kTmDQ, desc_add(dKm, kk * 16 * 128), desc_add(dSm, kk * 16 * 128), idQ, kk > 0);
+                mma_commit(&bar.dq_full);
+            }
+            if (ok) mma_commit(&bar.acc_done);
+        }
+    } else if (warp < kProdWarp) {
+        // --------------------------------------- P, dS (thread = key row)
+        const int half = warp / 4;             // query columns [32 half, 32 half + 32)
+        const int c0 = half * 32;
+        const int j = (warp % 4) * 32 + lane;  // key within the tile
+        const int key = n0 + j;
+        const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+        const uint32_t tS = tmem + kTmS + c0 + lane_off;
+        const uint32_t sDSrow = smem_u32(smem + kDSOff) + j * 128;
+        const float c2 = g.scale_log2;
+        bool ok = true;
+        for (int t = 0; t < n_it; ++t) {
+            const int st = t % QS;
+            const int i0 = ilo + (t % nqb) * BQ + c0;  // first query row of this half
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, t & 1, wd, 0xe0));
+            if (!ok) break;
+            tc_fence_after();
+            // (LSE / delta of stage st were written before q_full completed,
+            // which S^T_t itself waited for)
+            const float *lse2 = s_lse + st * BQ + c0;
+            const float *dlt = s_delta + st * BQ + c0;
+            const bool full = (i0 + 31 < s.Lq) && (n0 + BK - 1 < s.Lkv) &&
+                              (g.wr < 0 || n0 + BK - 1 <= i0 + g.wr) && (g.wl < 0 || n0 >= i0 + 31 - g.wl);
+            float p[32];
+            {
+                uint32_t sr[32];
+                tmem_ld32(tS, sr);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) p[c] = ex2(fmaf(__uint_as_float(sr[c]), c2, -lse2[c]));
+            }
+            if (!full) {
+                // queries that see this key: columns [clo, chi) of this half
+                int clo = 0, chi = min(32, s.Lq - i0);
+                if (g.wr >= 0) clo = max(clo, key - g.wr - i0);
+                if (g.wl >= 0) chi = min(chi, key + g.wl + 1 - i0);
+                if (key >= s.Lkv) chi = clo;
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (c < clo || c >= chi) p[c] = 0.f;
+            }
+            {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) pk[c] = pack2<T>(p[2 * c], p[2 * c + 1]);
+                tmem_st16(tS, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar.p_full);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full[t & 1], (t >> 1) & 1, wd, 0xe1));
+            if (!ok) break;
+            tc_fence_after();
+            // dS^T_t into shared memory (its buffer was last read by dK_{t-2}
+            // and dQ^T_{t-2}, issued before dP^T_t, whose completion we saw)
+            uint32_t dr[32];
+            tmem_ld32(tmem + kTmDP + (t & 1) * BQ + c0 + lane_off, dr);
+            const uint32_t dst = sDSrow + (t & 1) * kDSTile;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = cc * 8 + 2 * e;
+                    w[e] = pack2<T>(p[c] * (__uint_as_float(dr[c]) - dlt[c]),
+                                    p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]));
+                }
+                // 128B swizzle: 16-byte chunk (half * 4 + cc) of row j
+                st_shared_v4(dst + ((uint32_t)((half * 4 + cc) ^ (j & 7)) << 4), w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar.ds_full[t & 1]);
+        }
+        // epilogue: dK (scaled) from warps 0-3, dV from warps 4-7
+        if (ok && n_it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.acc_done, 0, wd, 0xe2));
+        tc_fence_after();
+        const MutView &ov = half == 0 ? a.dk : a.dv;
+        T *dstp = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss + (int64_t)hk * ov.sh;
+        const float mul = half == 0 ? g.scale : 1.f;
+        const uint32_t base = tmem + (half == 0 ? kTmDK : kTmDV) + lane_off;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t v[32];
+            if (n_it > 0) {
+                tmem_ld32(base + cc * 32, v);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+            if (j < nkeys) store_row32<T>(dstp + cc * 32, v, mul);
+        }
+    } else if (warp >= kDrainWarp0) {
+        // ----------------------------------- dQ^T drain (thread = head dim)
+        const int qd = warp % 4;  // TMEM lane quarter = head dims [32 qd, 32 qd + 32)
+        const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+        const uint32_t box = smem_u32(smem + kStgOff) + qd * kBox;
+        const int zb = g.thd ? 0 : b * g.Hq;
+        bool ok = true;
+        for (int t = 0; t < n_it; ++t) {
+            const int h = hk * g.G + t / nqb;
+            const int i0 = ilo + (t % nqb) * BQ;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dq_full, t & 1, wd, 0xf0));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[64];
+            tmem_ld32(tmem + kTmDQ + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tmem + kTmDQ + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tc_fence_before();
+            mbar_arrive(&bar.dq_free);
+            // the previous reduction must have read the box before it is rewritten
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            // box row r = query i0 + r, 32 fp32 (this warp's head dims) per row,
+            // 128B swizzle: 16-byte chunk (lane / 4) of row r at (lane / 4) ^ (r % 8)
+#pragma unroll
+            for (int r = 0; r < BQ; ++r)
+                st_shared_f32(box + r * 128 + ((uint32_t)((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4, v[r]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_reduce_add_3d(box, &tm_acc, qd * 32, s.q0 + i0, zb + h);
+                bulk_commit();
+            }
+        }
+        // the reductions must be complete before the CTA's shared memory goes away
+        if (lane == 0) bulk_wait0();
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// dq = scale * acc in the element type, acc laid out like LSE with D columns
+// per row.  8 head dims per thread (two 16-byte loads, one 16-byte store).
+template <typename T>
+__global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float *__restrict__ acc, Geometry g) {
+    constexpr int C = D / 8;
+    const int64_t rows = g.thd ? (int64_t)g.Hq * g.Tq : (int64_t)g.B * g.Hq * g.Sq;
+    const int64_t n = rows * C;
+    const int t_end = g.thd ? __ldg(g.cu_q + g.B) : 0;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = idx / C;
+        const int c = (int)(idx % C);
+        int b, h, srow;
+        if (g.thd) {
+            h = (int)(r / g.Tq);
+            srow = (int)(r % g.Tq);
+            b = 0;
+            if (srow >= t_end) continue;  // token rows outside every sequence are not written
+        } else {
+            const int64_t bhr = r / g.Sq;
+            srow = (int)(r % g.Sq);
+            b = (int)(bhr / g.Hq);
+            h = (int)(bhr % g.Hq);
+        }
+        const float4 *src = reinterpret_cast<const float4 *>(acc + r * D + c * 8);
+        const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+        uint4 y;
+        y.x = pack2<T>(x0.x * g.scale, x0.y * g.scale);
+        y.y = pack2<T>(x0.z * g.scale, x0.w * g.scale);
+        y.z = pack2<T>(x1.x * g.scale, x1.y * g.scale);
+        y.w = pack2<T>(x1.z * g.scale, x1.w * g.scale);
+        T *dst = (T *)dq.ptr + (int64_t)b * dq.sb + (int64_t)srow * dq.ss + (int64_t)h * dq.sh + c * 8;
+        *reinterpret_cast<uint4 *>(dst) = y;
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
+    const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+    const Geometry &g = a.g;
+    const uint64_t es = 2;
+    const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
+    uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
+    uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
+    auto strides = [&](const View &v, const uint64_t dims[4], uint64_t out[3]) {
+        const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
+        for (int i = 0; i < 3; ++i)
+            out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
+    };
+    const uint64_t acc_rows = g.thd ? (uint64_t)g.Tq : (uint64_t)g.Sq;
+    const uint64_t acc_heads = g.thd ? (uint64_t)g.Hq : (uint64_t)g.B * g.Hq;
+    cudaError_t e;
+    if (max_lkv > 0) {  // (no key at all: dk, dv are empty and dq = 0)
+        uint64_t sq[3], sk[3], sv[3], sd[3];
+        strides(a.q, dq, sq);
+        strides(a.k, dk, sk);
+        strides(a.v, dk, sv);
+        strides(a.dout, dq, sd);
+        CUtensorMap tq, tk, tv, tdo, tacc;
+        if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BQ)) != cudaSuccess) return e;
+        if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BK)) != cudaSuccess) return e;
+        if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BK)) != cudaSuccess) return e;
+        if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BQ)) != cudaSuccess) return e;
+        if ((e = make_tmap_f32_acc(&tacc, a.dq_acc, D, acc_rows, acc_heads, 32, BQ)) != cudaSuccess) return e;
+        auto kern = tc_bwd_fused_kernel<T>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
+            cudaSuccess)
+            return e;
+        const int n_ktiles = (max_lkv + BK - 1) / BK;
+        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
+        if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+        prof_before(st, kProfBwdFused);
+        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, a, n_ktiles);
+        prof_after(st);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const int64_t n = (int64_t)acc_rows * acc_heads * (D / 8);
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks > 0) {
+        prof_before(st, kProfBwdDqConvert);
+        dq_convert_kernel<T><<<(unsigned)blocks, 256, 0, st>>>(a.dq, a.dq_acc, g);
+        prof_after(st);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+bool uses_tc_bwd_fused(int dtype, int D_) { return (dtype == 0 || dtype == 1) && D_ == D; }
+
+cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, cudaStream_t st) {
+    // callers route problems without query rows to the two-kernel backward
+    if (a.g.D != D || !a.dq_acc || (a.g.thd ? a.g.Tq : a.g.Sq) <= 0) return cudaErrorInvalidValue;
+    switch (dtype) {
+        case 0: return launch_typed<__half>(a, max_lkv, st);
+        case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gbattn

@@ -30,8 +30,9 @@ def run_fwd(dprob):
     return o, lse
 
 
-def run_bwd(dprob, o, lse):
-    return gb.attn_bwd(dprob.dout, dprob.q, dprob.k, dprob.v, o, lse, **kw(dprob))
+def run_bwd(dprob, o, lse, deterministic=False):
+    return gb.attn_bwd(dprob.dout, dprob.q, dprob.k, dprob.v, o, lse, deterministic=deterministic,
+                       **kw(dprob))
 
 
 def rows_of(prob, t):

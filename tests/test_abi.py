@@ -38,6 +38,22 @@ def test_library_exports_every_declared_symbol(lib):
     assert not [s for s in exported if "gbattn" in s]
 
 
+def test_params_struct_matches_header():
+    """The ctypes attn_params has the header's fields, in the header's order."""
+    with open(os.path.join(ROOT, "include", "gbattn.h")) as f:
+        text = f.read()
+    body = text[text.index("typedef struct {\n    attn_dtype dtype;"):]
+    body = body[:body.index("} attn_params;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";")[:-1]:
+        decl = decl.strip().split("{", 1)[-1].strip()
+        parts = decl.replace("*", " ").split()
+        names += [n.strip(",") for n in parts[1:] if n.strip(",") and n != "const"
+                  and n not in ("int32_t", "int", "float")]
+    assert names == [f[0] for f in _lib.AttnParams._fields_]
+
+
 def _params(**kw):
     p = _lib.AttnParams()
     p.dtype, p.layout = _lib.ATTN_BF16, _lib.ATTN_LAYOUT_DENSE4D
@@ -56,6 +72,7 @@ def _t(ptr=4096, strides=(32768, 256, 64, 1)):
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(deterministic=2), _lib.ATTN_ERR_INVALID_ARG),
     (dict(D=96), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(D=0), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(Hq=3, Hkv=2), _lib.ATTN_ERR_INVALID_ARG),
@@ -104,6 +121,17 @@ def test_workspace_size(lib):
     assert n % 256 == 0
     p32 = _params(dtype=_lib.ATTN_F32)
     assert lib.attn_bwd_workspace_size(ctypes.byref(p32)) >= 4 * rows * p.Hq
+    # 16-bit, D = 128: the single pass adds an fp32 dq accumulator, the
+    # deterministic form needs the row terms only
+    for dt in (_lib.ATTN_F16, _lib.ATTN_BF16):
+        pf = _params(dtype=dt, D=128)
+        assert lib.attn_bwd_workspace_size(ctypes.byref(pf)) >= 4 * rows * pf.Hq * (1 + 128)
+        pf.deterministic = 1
+        nd = lib.attn_bwd_workspace_size(ctypes.byref(pf))
+        assert 4 * rows * pf.Hq <= nd < 4 * rows * pf.Hq + 256
+    pf = _params(dtype=_lib.ATTN_BF16, D=128)
+    pf.deterministic = 2
+    assert lib.attn_bwd_workspace_size(ctypes.byref(pf)) == 0
 
 
 def test_merge_rejects_bad_args(lib):

@@ -8,8 +8,8 @@ import torch
 
 import scaled_dot_product_03_gb300 as gb
 from scaled_dot_product_03_gb300 import inputs
-from gpu_helpers import (check_bwd, check_fwd, kw, lse_rows, rows_of, run_bwd, run_fwd,
-                         sample_keys, sample_rows)
+from gpu_helpers import (GRAD_FLOOR, check_bwd, check_fwd, kw, lse_rows, rows_of, run_bwd,
+                         run_fwd, sample_keys, sample_rows)
 from helpers import oracle_fwd, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -91,15 +91,16 @@ def test_dense_bf16_s1024_d64_fwd_bwd():
     check_bwd(prob, dq, dk, dv)
 
 
-@pytest.mark.parametrize("S", [1024, 2048, 4096, 8192, 16384])
-def test_dense_bf16_sweep_d128_sampled(S):
+@pytest.mark.parametrize("S,det", [(1024, False), (2048, False), (4096, False), (8192, False),
+                                   (16384, False), (4096, True)])
+def test_dense_bf16_sweep_d128_sampled(S, det):
     """16384 tokens per batch at head dim 128, the bench's launch shapes;
     compared on sampled rows (O, LSE, dq) and on the keys of two (batch, kv
-    head) units (dk, dv)."""
+    head) units (dk, dv).  det: the bitwise-reproducible backward."""
     prob = inputs.dense(16384 // S, S, 16, 128)
     d = _dev(prob)
     o, lse = run_fwd(d)
-    dq, dk, dv = run_bwd(d, o, lse)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
     _sync_ok()
     rows = sample_rows(prob, 48, seed=S)
     check_fwd(prob, o, lse, row_sel=rows)
@@ -108,11 +109,12 @@ def test_dense_bf16_sweep_d128_sampled(S):
     check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
 
 
-def test_varlen_thd_gqa_fwd_bwd_sampled():
+@pytest.mark.parametrize("det", [False, True])
+def test_varlen_thd_gqa_fwd_bwd_sampled(det):
     prob = inputs.varlen()
     d = _dev(prob)
     o, lse = run_fwd(d)
-    dq, dk, dv = run_bwd(d, o, lse)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
     _sync_ok()
     rows = sample_rows(prob, 64)
     check_fwd(prob, o, lse, row_sel=rows)
@@ -122,8 +124,15 @@ def test_varlen_thd_gqa_fwd_bwd_sampled():
 
 # ---------------------------------------------------------------- edge cases
 
-@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("D", [64, 128])
+# (dtype, D, deterministic): the 16-bit D=128 backward has a single-pass
+# and a two-kernel (bitwise reproducible) form; the others have one form.
+_EDGE_KINDS = [(torch.float16, 64, False), (torch.bfloat16, 64, False), (torch.float32, 64, False),
+               (torch.float16, 128, False), (torch.bfloat16, 128, False),
+               (torch.float32, 128, False), (torch.float16, 128, True),
+               (torch.bfloat16, 128, True)]
+
+
+@pytest.mark.parametrize("dtype,D,det", _EDGE_KINDS)
 @pytest.mark.parametrize("case", [
     dict(B=2, Sq=1, Skv=1, Hq=2, Hkv=1, window=(-1, 0)),
     dict(B=1, Sq=17, Skv=17, Hq=3, Hkv=3, window=(-1, -1)),
@@ -134,13 +143,13 @@ def test_varlen_thd_gqa_fwd_bwd_sampled():
     dict(B=1, Sq=260, Skv=260, Hq=2, Hkv=1, window=(5, 37)),    # two-sided window
     dict(B=1, Sq=150, Skv=90, Hq=2, Hkv=1, window=(0, 0)),      # rows >= 90 see nothing
 ])
-def test_edge_shapes_fwd_bwd(dtype, D, case):
+def test_edge_shapes_fwd_bwd(dtype, D, det, case):
     prob = inputs.dense(case["B"], case["Sq"], case["Hq"], D, dtype=dtype,
                         window=case["window"], Hkv=case["Hkv"], Skv=case["Skv"],
                         seed=case["Sq"] + D)
     d = _dev(prob)
     o, lse = run_fwd(d)
-    dq, dk, dv = run_bwd(d, o, lse)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
     _sync_ok()
     check_fwd(prob, o, lse)
     check_bwd(prob, dq, dk, dv)
@@ -203,6 +212,28 @@ def test_forward_is_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_backward_reproducibility():
+    """deterministic=True: bitwise equal on repeated runs.  Default single
+    pass: dk and dv (owned by one CTA each) bitwise equal, dq (fp32 sums in
+    scheduling order) equal to within fp32 rounding of the sums, and both
+    modes agree to the same precision."""
+    prob = inputs.dense(2, 1000, 8, 128, Hkv=2, seed=31, dout_seed=32)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    r1 = run_bwd(d, o, lse, deterministic=True)
+    r2 = run_bwd(d, o, lse, deterministic=True)
+    f1 = run_bwd(d, o, lse)
+    f2 = run_bwd(d, o, lse)
+    _sync_ok()
+    for a, b in zip(r1, r2):
+        assert torch.equal(a, b)
+    assert torch.equal(f1[1], f2[1]) and torch.equal(f1[2], f2[2])
+    for a, b in ((f1[0], f2[0]), (f1[0], r1[0]), (f1[1], r1[1]), (f1[2], r1[2])):
+        a64, b64 = a.double(), b.double()
+        scale = max(float(b64.abs().max()), GRAD_FLOOR)
+        assert float((a64 - b64).abs().max()) <= 1e-2 * scale
+
+
 def test_packed_gradient_buffer_views():
     """dq, dk, dv written into split views of one packed gradient buffer
     (the layout of the page-1 inputs) match separate buffers."""
@@ -213,8 +244,10 @@ def test_packed_gradient_buffer_views():
     g = torch.zeros_like(d.bases["qkv"])
     gq, gk, gv = g.split([16, 1, 1], dim=2)
     gq, gk, gv = (t.permute(1, 0, 2, 3) for t in (gq, gk, gv))
-    gb.attn_bwd(dout, d.q, d.k, d.v, o, lse, scale=0.1, window=(-1, 0), dq=gq, dk=gk, dv=gv)
-    dq, dk, dv = gb.attn_bwd(dout, d.q, d.k, d.v, o, lse, scale=0.1, window=(-1, 0))
+    gb.attn_bwd(dout, d.q, d.k, d.v, o, lse, scale=0.1, window=(-1, 0), dq=gq, dk=gk, dv=gv,
+                deterministic=True)
+    dq, dk, dv = gb.attn_bwd(dout, d.q, d.k, d.v, o, lse, scale=0.1, window=(-1, 0),
+                             deterministic=True)
     _sync_ok()
     assert torch.equal(gq, dq) and torch.equal(gk, dk) and torch.equal(gv, dv)
 
