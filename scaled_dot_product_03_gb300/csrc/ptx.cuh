@@ -139,6 +139,19 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// True in exactly one active lane of the (fully active) warp.  Issuing
+// tcgen05 work from an elected lane of a warp that otherwise runs in step
+// keeps the operands' arithmetic warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {

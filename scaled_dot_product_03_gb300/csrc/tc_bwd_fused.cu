@@ -7,27 +7,30 @@
 //   P^T  = exp(scale S^T - LSE)           recomputed from the forward's LSE
 //   dS^T = P^T o (dP^T - delta)           delta_i = <dO_i, O_i> (preprocess)
 //   dV  += P^T dO                         (P^T from TMEM)
-//   dK  += dS^T Q                         (dS^T from shared memory)
-//   dQ^T = K^T dS^T                       this block's share of dQ
+//   dK  += dS^T Q                         (dS^T from TMEM)
+//   dQ^T = K^T dS^T                       this block's share of dQ (dS^T
+//                                         from shared memory)
 // S and dP are formed once per (query, key) pair, so the pass executes the
 // five products of the method and nothing more.  dQ sums over every key
 // tile, i.e. over CTAs: each block's share is added into an fp32
-// accumulator in global memory with a TMA bulk reduce-add, and a small
-// kernel scales and converts the sums at the end.  The order of those fp32
-// additions depends on scheduling, so dQ is reproducible only to rounding;
-// dK and dV are owned by one CTA each.
+// accumulator in global memory with coalesced red.global.add (a warp adds
+// one 128-byte row segment per instruction, as fast as a TMA bulk reduce
+// and without staging through shared memory, whose bandwidth the MMA
+// operands already use up), and a small kernel scales and converts the sums
+// at the end.  The order of those fp32 additions depends on scheduling, so
+// dQ is reproducible only to rounding; dK and dV are owned by one CTA each.
 //
 // Warp roles (448 threads): warps 0-7 compute P and dS (thread = key row;
 // warps 0-3 take query columns 0-31 of the block, warps 4-7 columns 32-63)
 // and write dK / dV at the end; warp 8 issues TMA loads; warp 9 allocates
 // TMEM and issues the MMAs; warps 10-13 drain dQ^T from TMEM (thread = head
-// dim) into shared memory and issue the reductions, warp w owning head dims
+// dim) and add it into the accumulator, warp w owning head dims
 // [32 (w % 4), 32 (w % 4) + 32), which is the TMEM lane quarter it may read.
 //
-// TMEM columns (512): dK 0-127, dV 128-255, S^T / P^T 256-319, dP^T in two
-// buffers 320-383 and 384-447, dQ^T 448-511.  Shared memory: K, V (32 KB
-// each), three stages of Q and dO (16 KB each), two dS^T buffers (16 KB
-// each), the dQ staging boxes (32 KB) and the per-stage LSE / delta.
+// TMEM columns (512): dK 0-127, dV 128-255, S^T / P^T 256-319, dP^T / dS^T
+// in two buffers 320-383 and 384-447, dQ^T 448-511.  Shared memory: K, V
+// (32 KB each), three stages of Q and dO (16 KB each), two dS^T buffers
+// (16 KB each) and the per-stage LSE / delta.
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -54,14 +57,12 @@ constexpr int kDrain = 128;
 constexpr int kKVTile = BK * D * 2;   // 32 KB
 constexpr int kQTile = BQ * D * 2;    // 16 KB
 constexpr int kDSTile = BK * BQ * 2;  // 16 KB
-constexpr int kBox = BQ * 32 * 4;     // 8 KB: 64 rows x 32 fp32
 constexpr int kKOff = 0;
 constexpr int kVOff = kKOff + kKVTile;
 constexpr int kQOff = kVOff + kKVTile;
 constexpr int kDOOff = kQOff + QS * kQTile;
 constexpr int kDSOff = kDOOff + QS * kQTile;
-constexpr int kStgOff = kDSOff + 2 * kDSTile;
-constexpr int kStatOff = kStgOff + 4 * kBox;          // [QS][64] lse2, [QS][64] delta
+constexpr int kStatOff = kDSOff + 2 * kDSTile;       // [QS][64] lse2, [QS][64] delta
 constexpr int kBarOff = kStatOff + QS * BQ * 2 * 4;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;      // + barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -79,8 +80,8 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-// TMEM column of k-step kk (16 query columns) of packed P^T: columns 0-31 of
-// the block are packed into TMEM columns 0-15, 32-63 into 32-47.
+// TMEM column of k-step kk (16 query columns) of packed P^T or dS^T: columns
+// 0-31 of the block are packed into TMEM columns 0-15, 32-63 into 32-47.
 __device__ __forceinline__ constexpr uint32_t pcol(int kk) { return (kk / 2) * 32 + (kk % 2) * 8; }
 // Byte offset of k-step kk (16 head dims) in a K-major tile of `rows` rows.
 __device__ __forceinline__ constexpr uint32_t kmaj_off(int kk, int rows) {
@@ -107,21 +108,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
-__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ void red_add_f32(float *p, uint32_t v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(__uint_as_float(v)) : "memory");
 }
-
-// Adds a 64 x 32 fp32 box from shared memory into the tensor at (x, y, z).
-__device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const CUtensorMap *map, int x, int y, int z) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-            map),
-        "r"(x), "r"(y), "r"(z), "r"(src)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Writes 32 fp32 values (times mul) of one row as the element type.
 template <typename T>
@@ -140,7 +129,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                        const __grid_constant__ CUtensorMap tm_acc, BwdArgs a, int n_ktiles) {
+                        BwdArgs a, int n_ktiles) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -192,7 +181,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
-        prefetch_tmap(&tm_acc);
     }
     tc_fence_before();
     __syncthreads();
@@ -254,8 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Per block t: dV_t (once P_t is written), S^T_{t+1} (its TMEM held
         // P_t, read by dV_t just before: MMAs of one thread execute in issue
         // order), dP^T_{t+1} (into the other dP buffer), then dK_t and dQ^T_t
-        // once dS_t is in shared memory.
-        if (lane == 0 && n_it > 0) {
+        // once dS_t is in TMEM and shared memory.
+        // The whole warp runs the loop (waits, operand descriptors) in step;
+        // one elected lane issues each group of MMAs and its commit.
+        if (n_it > 0) {
             constexpr uint32_t idSP = idesc_f16(BK, BQ, kBf16, 0, 0);  // S^T, dP^T
             constexpr uint32_t idKV = idesc_f16(BK, D, kBf16, 0, 1);   // dV, dK: B = dO / Q, MN-major
             constexpr uint32_t idQ = idesc_f16(D, BQ, kBf16, 1, 1);    // dQ^T: A = K, B = dS^T, MN-major
@@ -265,24 +255,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dV = smem_desc_sw128(smem_u32(smem + kVOff), 16, 1024);
             // K as the MN-major A operand of dQ^T (M = head dim, two 64-wide atoms)
             const uint64_t dKm = smem_desc_sw128(smem_u32(smem + kKOff), BK * 128, 1024);
+            auto wait = [&](uint64_t *b, uint32_t ph, unsigned code) {
+                const bool r = __all_sync(0xffffffffu, mbar_wait(b, ph, wd, code));
+                if (r) tc_fence_after();
+                return r;
+            };
             auto issue_s = [&](int t) {
                 const uint64_t db = smem_desc_sw128(sQ + (t % QS) * kQTile, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + kTmS, desc_add(dK, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
-                mma_commit(&bar.s_full);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + kTmS, desc_add(dK, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP,
+                               kk > 0);
+                    mma_commit(&bar.s_full);
+                }
+                __syncwarp();
             };
             auto issue_dp = [&](int t) {
                 const uint64_t db = smem_desc_sw128(sDO + (t % QS) * kQTile, 16, 1024);
+                const uint32_t dst = tmem + kTmDP + (t & 1) * BQ;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + kTmDP + (t & 1) * BQ, desc_add(dV, kmaj_off(kk, BK)),
-                           desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
-                mma_commit(&bar.dp_full[t & 1]);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(dst, desc_add(dV, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
+                    mma_commit(&bar.dp_full[t & 1]);
+                }
+                __syncwarp();
             };
-            bool ok = mbar_wait(&bar.kv_full, 0, wd, 0xd0) && mbar_wait(&bar.q_full[0], 0, wd, 0xd1);
+            bool ok = wait(&bar.kv_full, 0, 0xd0) && wait(&bar.q_full[0], 0, 0xd1);
             if (ok) {
-                tc_fence_after();
                 issue_s(0);
                 issue_dp(0);
             }
@@ -292,37 +293,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Q_t / dO_t as MN-major B operands (N = head dim, two 64-wide atoms)
                 const uint64_t dOm = smem_desc_sw128(sDO + st * kQTile, BQ * 128, 1024);
                 const uint64_t dQm = smem_desc_sw128(sQ + st * kQTile, BQ * 128, 1024);
-                if (!(ok = mbar_wait(&bar.p_full, t & 1, wd, 0xd2))) break;
-                tc_fence_after();
+                const uint32_t acc0 = t > 0 ? 1u : 0u;
+                if (!(ok = wait(&bar.p_full, t & 1, 0xd2))) break;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + kTmDV, tmem + kTmS + pcol(kk), desc_add(dOm, kk * 16 * 128), idKV,
-                           (t > 0 || kk > 0));
+                    for (int kk = 0; kk < BQ / 16; ++kk)
+                        mma_ts(tmem + kTmDV, tmem + kTmS + pcol(kk), desc_add(dOm, kk * 16 * 128), idKV,
+                               kk > 0 ? 1u : acc0);
+                }
+                __syncwarp();
                 if (next) {
-                    if (!(ok = mbar_wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, wd, 0xd3))) break;
-                    tc_fence_after();
+                    if (!(ok = wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, 0xd3))) break;
                     issue_s(t + 1);
                     issue_dp(t + 1);
                 }
-                if (!(ok = mbar_wait(&bar.ds_full[t & 1], (t >> 1) & 1, wd, 0xd4))) break;
-                tc_fence_after();
-                // dS^T_t: K-major A of dK (K = queries), MN-major B of dQ^T (N = queries)
-                const uint32_t sds = sDS + (t & 1) * kDSTile;
-                const uint64_t dS = smem_desc_sw128(sds, 16, 1024);
-                const uint64_t dSm = smem_desc_sw128(sds, BK * 128, 1024);
+                if (!(ok = wait(&bar.ds_full[t & 1], (t >> 1) & 1, 0xd4))) break;
+                // dS^T_t: A of dK from TMEM (packed over dP^T_t), MN-major B of
+                // dQ^T from shared memory (N = queries)
+                const uint64_t dSm = smem_desc_sw128(sDS + (t & 1) * kDSTile, BK * 128, 1024);
+                const uint32_t tds = tmem + kTmDP + (t & 1) * BQ;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ss(tmem + kTmDK, desc_add(dS, kk * 32), desc_add(dQm, kk * 16 * 128), idKV,
-                           (t > 0 || kk > 0));
-                mma_commit(&bar.q_empty[st]);
-                if (t > 0 && !(ok = mbar_wait(&bar.dq_free, (t - 1) & 1, wd, 0xd5))) break;
-                tc_fence_after();
+                    for (int kk = 0; kk < BQ / 16; ++kk)
+                        mma_ts(tmem + kTmDK, tds + pcol(kk), desc_add(dQm, kk * 16 * 128), idKV, kk > 0 ? 1u : acc0);
+                    mma_commit(&bar.q_empty[st]);
+                }
+                __syncwarp();
+                if (t > 0 && !(ok = wait(&bar.dq_free, (t - 1) & 1, 0xd5))) break;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_ss(tmem + kTmDQ, desc_add(dKm, kk * 16 * 128), desc_add(dSm, kk * 16 * 128), idQ, kk > 0);
-                mma_commit(&bar.dq_full);
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_ss(tmem + kTmDQ, desc_add(dKm, kk * 16 * 128), desc_add(dSm, kk * 16 * 128), idQ, kk > 0);
+                    mma_commit(&bar.dq_full);
+                }
+                __syncwarp();
             }
-            if (ok) mma_commit(&bar.acc_done);
+            if (ok && elect_one()) mma_commit(&bar.acc_done);
+            __syncwarp();
         }
     } else if (warp < kProdWarp) {
         // --------------------------------------- P, dS (thread = key row)
@@ -376,23 +383,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full[t & 1], (t >> 1) & 1, wd, 0xe1));
             if (!ok) break;
             tc_fence_after();
-            // dS^T_t into shared memory (its buffer was last read by dK_{t-2}
-            // and dQ^T_{t-2}, issued before dP^T_t, whose completion we saw)
-            uint32_t dr[32];
-            tmem_ld32(tmem + kTmDP + (t & 1) * BQ + c0 + lane_off, dr);
+            // dS^T_t packed over dP^T_t in TMEM (A of dK) and into shared memory
+            // (B of dQ^T; the buffer was last read by dQ^T_{t-2}, issued
+            // before dP^T_t, whose completion we saw)
+            const uint32_t tDP = tmem + kTmDP + (t & 1) * BQ + c0 + lane_off;
+            uint32_t pk[16];
+            {
+                uint32_t dr[32];
+                tmem_ld32(tDP, dr);
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    pk[c] = pack2<T>(p[2 * c] * (__uint_as_float(dr[2 * c]) - dlt[2 * c]),
+                                     p[2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dlt[2 * c + 1]));
+            }
+            tmem_st16(tDP, pk);
             const uint32_t dst = sDSrow + (t & 1) * kDSTile;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = cc * 8 + 2 * e;
-                    w[e] = pack2<T>(p[c] * (__uint_as_float(dr[c]) - dlt[c]),
-                                    p[c + 1] * (__uint_as_float(dr[c + 1]) - dlt[c + 1]));
-                }
-                // 128B swizzle: 16-byte chunk (half * 4 + cc) of row j
-                st_shared_v4(dst + ((uint32_t)((half * 4 + cc) ^ (j & 7)) << 4), w[0], w[1], w[2], w[3]);
-            }
+            for (int cc = 0; cc < 4; ++cc)  // 128B swizzle: 16-byte chunk (half * 4 + cc) of row j
+                st_shared_v4(dst + ((uint32_t)((half * 4 + cc) ^ (j & 7)) << 4), pk[4 * cc], pk[4 * cc + 1],
+                             pk[4 * cc + 2], pk[4 * cc + 3]);
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar.ds_full[t & 1]);
@@ -419,8 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ----------------------------------- dQ^T drain (thread = head dim)
         const int qd = warp % 4;  // TMEM lane quarter = head dims [32 qd, 32 qd + 32)
         const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-        const uint32_t box = smem_u32(smem + kStgOff) + qd * kBox;
-        const int zb = g.thd ? 0 : b * g.Hq;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int h = hk * g.G + t / nqb;
@@ -433,24 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + kTmDQ + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
             tc_fence_before();
             mbar_arrive(&bar.dq_free);
-            // the previous reduction must have read the box before it is rewritten
-            if (lane == 0) bulk_wait_read0();
-            __syncwarp();
-            // box row r = query i0 + r, 32 fp32 (this warp's head dims) per row,
-            // 128B swizzle: 16-byte chunk (lane / 4) of row r at (lane / 4) ^ (r % 8)
+            // row i0 + r of the accumulator (laid out like LSE, D floats per
+            // row); rows past the sequence are skipped (their dS is 0, and the
+            // last head's would lie past the array)
+            float *acc = a.dq_acc + lse_index(g, s, b, h, i0) * D + qd * 32 + lane;
+            const int nr = min(BQ, s.Lq - i0);
 #pragma unroll
             for (int r = 0; r < BQ; ++r)
-                st_shared_f32(box + r * 128 + ((uint32_t)((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4, v[r]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_reduce_add_3d(box, &tm_acc, qd * 32, s.q0 + i0, zb + h);
-                bulk_commit();
-            }
+                if (r < nr) red_add_f32(acc + r * D, v[r]);
         }
-        // the reductions must be complete before the CTA's shared memory goes away
-        if (lane == 0) bulk_wait0();
-        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -519,12 +518,11 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         strides(a.k, dk, sk);
         strides(a.v, dk, sv);
         strides(a.dout, dq, sd);
-        CUtensorMap tq, tk, tv, tdo, tacc;
+        CUtensorMap tq, tk, tv, tdo;
         if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BQ)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BK)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BK)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BQ)) != cudaSuccess) return e;
-        if ((e = make_tmap_f32_acc(&tacc, a.dq_acc, D, acc_rows, acc_heads, 32, BQ)) != cudaSuccess) return e;
         auto kern = tc_bwd_fused_kernel<T>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
             cudaSuccess)
@@ -533,7 +531,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdFused);
-        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, a, n_ktiles);
+        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
