@@ -218,61 +218,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Per block t: S^T_t, dP^T_t, then dV_t (once P is written), S^T_{t+1}
         // (its TMEM held P_t, read by dV_t just before: MMAs of one thread
         // execute in issue order), dK_t (once dS is written), dP^T_{t+1}.
-        if (lane == 0 && n_it > 0) {
+        // The whole warp runs the loop in step; one elected lane issues each
+        // group of MMAs with its commit.
+        if (n_it > 0) {
             constexpr uint32_t idSP = idesc_f16(BLK, BLK, kBf16, 0, 0);  // S^T, dP^T
             constexpr uint32_t idKV = idesc_f16(BLK, D, kBf16, 0, 1);    // dV, dK
             const uint32_t sQ = smem_u32(smem + C::kQOff), sDO = smem_u32(smem + C::kDOOff);
             const uint64_t dK = smem_desc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
             const uint64_t dV = smem_desc_sw128(smem_u32(smem + C::kVOff), 16, 1024);
+            auto wait = [&](uint64_t *b, uint32_t ph, unsigned code) {
+                const bool r = __all_sync(0xffffffffu, mbar_wait(b, ph, wd, code));
+                if (r) tc_fence_after();
+                return r;
+            };
             auto issue_s = [&](int t) {
                 const uint64_t db = smem_desc_sw128(sQ + (t % QS) * C::kTile, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::kTmS, desc_add(dK, kmaj_off(kk, BLK)), desc_add(db, kmaj_off(kk, BLK)),
-                           idSP, kk > 0);
-                mma_commit(&bar.s_full);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + C::kTmS, desc_add(dK, kmaj_off(kk, BLK)), desc_add(db, kmaj_off(kk, BLK)),
+                               idSP, kk > 0);
+                    mma_commit(&bar.s_full);
+                }
+                __syncwarp();
             };
             auto issue_dp = [&](int t) {
                 const uint64_t db = smem_desc_sw128(sDO + (t % QS) * C::kTile, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + C::kTmDP, desc_add(dV, kmaj_off(kk, BLK)), desc_add(db, kmaj_off(kk, BLK)),
-                           idSP, kk > 0);
-                mma_commit(&bar.dp_full);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + C::kTmDP, desc_add(dV, kmaj_off(kk, BLK)), desc_add(db, kmaj_off(kk, BLK)),
+                               idSP, kk > 0);
+                    mma_commit(&bar.dp_full);
+                }
+                __syncwarp();
             };
-            bool ok = mbar_wait(&bar.kv_full, 0, wd, 0x50) && mbar_wait(&bar.q_full[0], 0, wd, 0x51);
+            bool ok = wait(&bar.kv_full, 0, 0x50) && wait(&bar.q_full[0], 0, 0x51);
             if (ok) {
-                tc_fence_after();
                 issue_s(0);
                 issue_dp(0);
             }
             for (int t = 0; ok && t < n_it; ++t) {
                 const int st = t % QS;
                 const bool next = t + 1 < n_it;
+                const uint32_t acc0 = t > 0 ? 1u : 0u;
                 // B operands as MN-major (N = head dim) views of the Q / dO tiles
                 const uint64_t dOm = smem_desc_sw128(sDO + st * C::kTile, BLK * 128, 1024);
                 const uint64_t dQm = smem_desc_sw128(sQ + st * C::kTile, BLK * 128, 1024);
-                if (!(ok = mbar_wait(&bar.p_full, t & 1, wd, 0x52))) break;
-                tc_fence_after();
+                if (!(ok = wait(&bar.p_full, t & 1, 0x52))) break;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < BLK / 16; ++kk)
-                    mma_ts(tmem + C::kTmDV, tmem + C::kTmS + pcol(kk), desc_add(dOm, kk * 16 * 128), idKV,
-                           (t > 0 || kk > 0));
+                    for (int kk = 0; kk < BLK / 16; ++kk)
+                        mma_ts(tmem + C::kTmDV, tmem + C::kTmS + pcol(kk), desc_add(dOm, kk * 16 * 128), idKV,
+                               kk > 0 ? 1u : acc0);
+                }
+                __syncwarp();
                 if (next) {
-                    if (!(ok = mbar_wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, wd, 0x53))) break;
-                    tc_fence_after();
+                    if (!(ok = wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, 0x53))) break;
                     issue_s(t + 1);
                 }
-                if (!(ok = mbar_wait(&bar.ds_full, t & 1, wd, 0x54))) break;
-                tc_fence_after();
+                if (!(ok = wait(&bar.ds_full, t & 1, 0x54))) break;
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < BLK / 16; ++kk)
-                    mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + pcol(kk), desc_add(dQm, kk * 16 * 128), idKV,
-                           (t > 0 || kk > 0));
-                mma_commit(&bar.q_empty[st]);
+                    for (int kk = 0; kk < BLK / 16; ++kk)
+                        mma_ts(tmem + C::kTmDK, tmem + C::kTmDP + pcol(kk), desc_add(dQm, kk * 16 * 128), idKV,
+                               kk > 0 ? 1u : acc0);
+                    mma_commit(&bar.q_empty[st]);
+                }
+                __syncwarp();
                 if (next) issue_dp(t + 1);
             }
-            if (ok) mma_commit(&bar.acc_done);
+            if (ok && elect_one()) mma_commit(&bar.acc_done);
+            __syncwarp();
         }
     } else {
         // --------------------------------------- P, dS (thread = key row)
@@ -497,25 +514,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Per block: S of the next block as soon as this block's S has been
         // read, dQ += dS K, then dP of the next block (its TMEM held dS, read
         // by the dQ MMA just before; MMAs of one thread run in issue order).
-        if (lane == 0) {
+        // The whole warp runs the loop in step; one elected lane issues each
+        // group of MMAs with its commit.
+        {
             constexpr uint32_t idS = idesc_f16(BLK, BLK, kBf16, 0, 0);  // S, dP: A from TMEM
             constexpr uint32_t idQ = idesc_f16(BLK, D, kBf16, 0, 1);    // dQ: B = K, MN-major
             const uint32_t sK = smem_u32(smem + C::kKOff), sV = smem_u32(smem + C::kVOff);
+            auto wait = [&](uint64_t *b, uint32_t ph, unsigned code) {
+                const bool r = __all_sync(0xffffffffu, mbar_wait(b, ph, wd, code));
+                if (r) tc_fence_after();
+                return r;
+            };
+            auto commit = [&](uint64_t *b) {
+                if (elect_one()) mma_commit(b);
+                __syncwarp();
+            };
             auto issue_s = [&](int gbk) {
                 const uint64_t db = smem_desc_sw128(sK + (gbk % KS) * C::kTile, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
-                           kk > 0);
-                mma_commit(&bar.s_full);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ts(tmem + C::kTmS, tmem + C::kTmQ + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
+                               kk > 0);
+                    mma_commit(&bar.s_full);
+                }
+                __syncwarp();
             };
             auto issue_dp = [&](int gbk) {
                 const uint64_t db = smem_desc_sw128(sV + (gbk % KS) * C::kTile, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
-                           kk > 0);
-                mma_commit(&bar.dp_full);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ts(tmem + C::kTmDP, tmem + C::kTmDO + kk * 8, desc_add(db, kmaj_off(kk, BLK)), idS,
+                               kk > 0);
+                    mma_commit(&bar.dp_full);
+                }
+                __syncwarp();
             };
             int gb = 0, tn = 0;  // key blocks and non-empty items so far
             bool ok = true;
@@ -524,12 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tl.nb == 0) continue;
                 // Q and dO of this item are in TMEM (written after the previous
                 // item's MMAs had all completed)
-                if (!(ok = mbar_wait(&bar.qd_ready, tn & 1, wd, 0x90))) break;
-                if (!(ok = mbar_wait(&bar.k_full[gb % KS], (gb / KS) & 1, wd, 0x91))) break;
-                tc_fence_after();
+                if (!(ok = wait(&bar.qd_ready, tn & 1, 0x90))) break;
+                if (!(ok = wait(&bar.k_full[gb % KS], (gb / KS) & 1, 0x91))) break;
                 issue_s(gb);
-                if (!(ok = mbar_wait(&bar.v_full[gb % KS], (gb / KS) & 1, wd, 0x92))) break;
-                tc_fence_after();
+                if (!(ok = wait(&bar.v_full[gb % KS], (gb / KS) & 1, 0x92))) break;
                 issue_dp(gb);
                 for (int jb = 0; ok && jb < tl.nb; ++jb) {
                     const int gbk = gb + jb, st = gbk % KS;
@@ -537,28 +569,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st1 = (gbk + 1) % KS;
                     const uint32_t ph1 = ((gbk + 1) / KS) & 1;
                     if (next) {
-                        if (!(ok = mbar_wait(&bar.k_full[st1], ph1, wd, 0x93))) break;
-                        if (!(ok = mbar_wait(&bar.s_free, gbk & 1, wd, 0x94))) break;
-                        tc_fence_after();
+                        if (!(ok = wait(&bar.k_full[st1], ph1, 0x93))) break;
+                        if (!(ok = wait(&bar.s_free, gbk & 1, 0x94))) break;
                         issue_s(gbk + 1);
                     }
-                    if (!(ok = mbar_wait(&bar.ds_full, gbk & 1, wd, 0x95))) break;
-                    tc_fence_after();
+                    if (!(ok = wait(&bar.ds_full, gbk & 1, 0x95))) break;
                     const uint64_t dKm = smem_desc_sw128(sK + st * C::kTile, BLK * 128, 1024);
+                    const uint32_t acc0 = jb > 0 ? 1u : 0u;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < BLK / 16; ++kk)
-                        mma_ts(tmem + C::kTmDQ, tmem + C::kTmDP + pcol(kk), desc_add(dKm, kk * 16 * 128), idQ,
-                               (jb > 0 || kk > 0));
-                    mma_commit(&bar.k_empty[st]);
-                    mma_commit(&bar.v_empty[st]);
+                        for (int kk = 0; kk < BLK / 16; ++kk)
+                            mma_ts(tmem + C::kTmDQ, tmem + C::kTmDP + pcol(kk), desc_add(dKm, kk * 16 * 128), idQ,
+                                   kk > 0 ? 1u : acc0);
+                        mma_commit(&bar.k_empty[st]);
+                        mma_commit(&bar.v_empty[st]);
+                    }
+                    __syncwarp();
                     if (next) {
-                        if (!(ok = mbar_wait(&bar.v_full[st1], ph1, wd, 0x96))) break;
-                        tc_fence_after();
+                        if (!(ok = wait(&bar.v_full[st1], ph1, 0x96))) break;
                         issue_dp(gbk + 1);
                     }
                 }
                 if (!ok) break;
-                mma_commit(&bar.dq_done);
+                commit(&bar.dq_done);
                 gb += tl.nb;
                 ++tn;
             }

@@ -196,56 +196,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the TMEM that P_i(jb) occupies; MMAs issued by one thread execute in
         // issue order, so it is written only after PV_i(jb) has read P.
         // Descriptors are formed once; each MMA adds a compile-time offset.
-        if (lane == 0 && nb > 0) {
+        // The whole warp runs the loop in step (waits, descriptors) and one
+        // elected lane issues each group of MMAs with its commit.
+        if (nb > 0) {
             constexpr uint32_t idS = idesc_f16(BM, BN, kBf16, 0, 0);
             constexpr uint32_t idPV = idesc_f16(BM, D, kBf16, 0, 1);
             const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024);
+            auto wait = [&](uint64_t *b, uint32_t ph, unsigned code) {
+                const bool r = __all_sync(0xffffffffu, mbar_wait(b, ph, wd, code));
+                if (r) tc_fence_after();
+                return r;
+            };
             auto issue_s = [&](int i, int jb) {  // S_i = Q_i K_jb^T
                 const int st = jb % KS;
                 const uint64_t da = desc_add(dQ, i * C::kTileBytes);
                 const uint64_t db = smem_desc_sw128(sK + st * C::kTileBytes, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    constexpr int kRow = BM * 128;
-                    const uint32_t off = (kk / 4) * kRow + (kk % 4) * 32;
-                    mma_ss(tmem + i * BN, desc_add(da, off), desc_add(db, off), idS, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        constexpr int kRow = BM * 128;
+                        const uint32_t off = (kk / 4) * kRow + (kk % 4) * 32;
+                        mma_ss(tmem + i * BN, desc_add(da, off), desc_add(db, off), idS, kk > 0);
+                    }
+                    mma_commit(&bar.s_full[i]);
                 }
-                mma_commit(&bar.s_full[i]);
+                __syncwarp();
+            };
+            auto commit = [&](uint64_t *b) {
+                if (elect_one()) mma_commit(b);
+                __syncwarp();
             };
             auto in_range = [&](int i, int jb) { return jb >= tr[i].blo && jb < tr[i].bhi; };
-            bool ok = mbar_wait(&bar.q_full, 0, wd, 0x20) && mbar_wait(&bar.k_full[0], 0, wd, 0x21);
+            bool ok = wait(&bar.q_full, 0, 0x20) && wait(&bar.k_full[0], 0, 0x21);
             if (ok) {
-                tc_fence_after();
+#pragma unroll
                 for (int i = 0; i < NQ; ++i)
                     if (in_range(i, 0)) issue_s(i, 0);
-                mma_commit(&bar.k_empty[0]);
+                commit(&bar.k_empty[0]);
             }
             for (int jb = 0; ok && jb < nb; ++jb) {
                 const int st = jb % KS;
                 const uint32_t ph = (jb / KS) & 1;
                 const bool has_next = jb + 1 < nb;
-                if (!(ok = mbar_wait(&bar.v_full[st], ph, wd, 0x23))) break;
-                if (has_next &&
-                    !(ok = mbar_wait(&bar.k_full[(jb + 1) % KS], ((jb + 1) / KS) & 1, wd, 0x22)))
-                    break;
-                tc_fence_after();
+                if (!(ok = wait(&bar.v_full[st], ph, 0x23))) break;
+                if (has_next && !(ok = wait(&bar.k_full[(jb + 1) % KS], ((jb + 1) / KS) & 1, 0x22))) break;
                 const uint64_t dv = smem_desc_sw128(sV + st * C::kTileBytes, BN * 128, 1024);
+#pragma unroll
                 for (int i = 0; i < NQ; ++i) {
                     if (in_range(i, jb)) {
                         const int t = jb - tr[i].blo;
-                        if (!(ok = mbar_wait(&bar.p_full[i], t & 1, wd, 0x24))) break;
-                        tc_fence_after();
+                        if (!(ok = wait(&bar.p_full[i], t & 1, 0x24))) break;
+                        const uint32_t acc0 = t > 0 ? 1u : 0u;
+                        if (elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8,
-                                   desc_add(dv, kk * 16 * 128), idPV, (t > 0 || kk > 0));
-                        mma_commit(&bar.pv_done[i]);
+                            for (int kk = 0; kk < BN / 16; ++kk)
+                                mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8, desc_add(dv, kk * 16 * 128),
+                                       idPV, kk > 0 ? 1u : acc0);
+                            mma_commit(&bar.pv_done[i]);
+                        }
+                        __syncwarp();
                     }
                     if (has_next && in_range(i, jb + 1)) issue_s(i, jb + 1);
                 }
                 if (!ok) break;
-                mma_commit(&bar.v_empty[st]);
-                if (has_next) mma_commit(&bar.k_empty[(jb + 1) % KS]);
+                commit(&bar.v_empty[st]);
+                if (has_next) commit(&bar.k_empty[(jb + 1) % KS]);
             }
         }
     } else {
