@@ -12,25 +12,25 @@
 //                                         from shared memory)
 // S and dP are formed once per (query, key) pair, so the pass executes the
 // five products of the method and nothing more.  dQ sums over every key
-// tile, i.e. over CTAs: each block's share is added into an fp32
-// accumulator in global memory with coalesced red.global.add (a warp adds
-// one 128-byte row segment per instruction, as fast as a TMA bulk reduce
-// and without staging through shared memory, whose bandwidth the MMA
-// operands already use up), and a small kernel scales and converts the sums
-// at the end.  The order of those fp32 additions depends on scheduling, so
+// tile, i.e. over CTAs: each block's share is staged in shared memory and
+// added into an fp32 accumulator in global memory with TMA bulk
+// reduce-adds (one instruction per 8 KB box; per-element red.global, as fast
+// at the L2, costs the draining warps about 1 us of issue per block), and a
+// small kernel scales and converts the sums at the end.  The order of those fp32 additions depends on scheduling, so
 // dQ is reproducible only to rounding; dK and dV are owned by one CTA each.
 //
 // Warp roles (448 threads): warps 0-7 compute P and dS (thread = key row;
 // warps 0-3 take query columns 0-31 of the block, warps 4-7 columns 32-63)
 // and write dK / dV at the end; warp 8 issues TMA loads; warp 9 allocates
 // TMEM and issues the MMAs; warps 10-13 drain dQ^T from TMEM (thread = head
-// dim) and add it into the accumulator, warp w owning head dims
-// [32 (w % 4), 32 (w % 4) + 32), which is the TMEM lane quarter it may read.
+// dim) into shared memory and issue the reductions, warp w owning head dims
+// [32 (w % 4), 32 (w % 4) + 32), which is the TMEM lane quarter it may read,
+// and one 64 x 32 fp32 staging box.
 //
 // TMEM columns (512): dK 0-127, dV 128-255, S^T / P^T 256-319, dP^T / dS^T
 // in two buffers 320-383 and 384-447, dQ^T 448-511.  Shared memory: K, V
 // (32 KB each), three stages of Q and dO (16 KB each), two dS^T buffers
-// (16 KB each) and the per-stage LSE / delta.
+// (16 KB each), the dQ staging boxes (32 KB) and the per-stage LSE / delta.
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -57,12 +57,14 @@ constexpr int kDrain = 128;
 constexpr int kKVTile = BK * D * 2;   // 32 KB
 constexpr int kQTile = BQ * D * 2;    // 16 KB
 constexpr int kDSTile = BK * BQ * 2;  // 16 KB
+constexpr int kBox = BQ * 32 * 4;     // 8 KB: 64 rows x 32 fp32
 constexpr int kKOff = 0;
 constexpr int kVOff = kKOff + kKVTile;
 constexpr int kQOff = kVOff + kKVTile;
 constexpr int kDOOff = kQOff + QS * kQTile;
 constexpr int kDSOff = kDOOff + QS * kQTile;
-constexpr int kStatOff = kDSOff + 2 * kDSTile;       // [QS][64] lse2, [QS][64] delta
+constexpr int kStgOff = kDSOff + 2 * kDSTile;
+constexpr int kStatOff = kStgOff + 4 * kBox;          // [QS][64] lse2, [QS][64] delta
 constexpr int kBarOff = kStatOff + QS * BQ * 2 * 4;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;      // + barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -108,9 +110,21 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
-__device__ __forceinline__ void red_add_f32(float *p, uint32_t v) {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(__uint_as_float(v)) : "memory");
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+
+// Adds a 64 x 32 fp32 box from shared memory into the tensor at (x, y, z).
+__device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const CUtensorMap *map, int x, int y, int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            map),
+        "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Writes 32 fp32 values (times mul) of one row as the element type.
 template <typename T>
@@ -129,7 +143,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                        BwdArgs a, int n_ktiles) {
+                        const __grid_constant__ CUtensorMap tm_acc, BwdArgs a, int n_ktiles) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -181,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_acc);
     }
     tc_fence_before();
     __syncthreads();
@@ -429,6 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ----------------------------------- dQ^T drain (thread = head dim)
         const int qd = warp % 4;  // TMEM lane quarter = head dims [32 qd, 32 qd + 32)
         const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+        const uint32_t box = smem_u32(smem + kStgOff) + qd * kBox;
+        const int zb = g.thd ? 0 : b * g.Hq;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
             const int h = hk * g.G + t / nqb;
@@ -441,15 +458,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + kTmDQ + 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
             tc_fence_before();
             mbar_arrive(&bar.dq_free);
-            // row i0 + r of the accumulator (laid out like LSE, D floats per
-            // row); rows past the sequence are skipped (their dS is 0, and the
-            // last head's would lie past the array)
-            float *acc = a.dq_acc + lse_index(g, s, b, h, i0) * D + qd * 32 + lane;
-            const int nr = min(BQ, s.Lq - i0);
+            // the previous reduction must have read the box before it is rewritten
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            // box row r = query i0 + r, 32 fp32 (this warp's head dims) per row,
+            // 128B swizzle: 16-byte chunk (lane / 4) of row r at (lane / 4) ^ (r % 8)
 #pragma unroll
             for (int r = 0; r < BQ; ++r)
-                if (r < nr) red_add_f32(acc + r * D, v[r]);
+                st_shared_f32(box + r * 128 + ((uint32_t)((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4, v[r]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            // rows past the tensor's end are dropped by the copy; rows past a
+            // THD sequence add the 0s of their masked dS to the next sequence
+            if (lane == 0) {
+                tma_reduce_add_3d(box, &tm_acc, qd * 32, s.q0 + i0, zb + h);
+                bulk_commit();
+            }
         }
+        // the reductions must be complete before the CTA's shared memory goes away
+        if (lane == 0) bulk_wait0();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -518,11 +546,12 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         strides(a.k, dk, sk);
         strides(a.v, dk, sv);
         strides(a.dout, dq, sd);
-        CUtensorMap tq, tk, tv, tdo;
+        CUtensorMap tq, tk, tv, tdo, tacc;
         if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BQ)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BK)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BK)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BQ)) != cudaSuccess) return e;
+        if ((e = make_tmap_f32_acc(&tacc, a.dq_acc, D, acc_rows, acc_heads, 32, BQ)) != cudaSuccess) return e;
         auto kern = tc_bwd_fused_kernel<T>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
             cudaSuccess)
@@ -531,7 +560,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdFused);
-        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, a, n_ktiles);
+        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

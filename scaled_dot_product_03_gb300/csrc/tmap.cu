@@ -40,4 +40,19 @@ cudaError_t make_tmap_16bit(CUtensorMap *map, const void *ptr, int dtype, const 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_f32_acc(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, uint64_t heads,
+                              uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if (box_cols * 4 != 128) return cudaErrorInvalidValue;
+    cuuint64_t gdim[3] = {cols, rows, heads};
+    cuuint64_t gstride[2] = {cols * 4, rows * cols * 4};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace gbattn

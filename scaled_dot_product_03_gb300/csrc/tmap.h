@@ -14,4 +14,10 @@ namespace gbattn {
 cudaError_t make_tmap_16bit(CUtensorMap *map, const void *ptr, int dtype, const uint64_t dims[4],
                             const uint64_t strides_bytes[3], uint32_t box_rows);
 
+// 3-D tiled tensor map over a contiguous fp32 array [heads][rows][cols]
+// (cols innermost), 128-byte swizzle, box {box_cols, box_rows, 1}; used as
+// the target of bulk reduce-adds.  box_cols * 4 must be 128.
+cudaError_t make_tmap_f32_acc(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, uint64_t heads,
+                              uint32_t box_cols, uint32_t box_rows);
+
 }  // namespace gbattn
