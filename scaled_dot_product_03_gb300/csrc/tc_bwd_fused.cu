@@ -21,7 +21,8 @@
 //
 // Warp roles (448 threads): warps 0-7 compute P and dS (thread = key row;
 // warps 0-3 take query columns 0-31 of the block, warps 4-7 columns 32-63)
-// and write dK / dV at the end; warp 8 issues TMA loads; warp 9 allocates
+// and write dK / dV at the end (staged in the then idle K / V tiles and
+// written with TMA stores); warp 8 issues TMA loads; warp 9 allocates
 // TMEM and issues the MMAs; warps 10-13 drain dQ^T from TMEM (thread = head
 // dim) into shared memory and issue the reductions, warp w owning head dims
 // [32 (w % 4), 32 (w % 4) + 32), which is the TMEM lane quarter it may read,
@@ -122,9 +123,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const CUtensorMa
         "r"(x), "r"(y), "r"(z), "r"(src)
         : "memory");
 }
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Writes 32 fp32 values (times mul) of one row as the element type.
 template <typename T>
@@ -143,7 +141,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                        const __grid_constant__ CUtensorMap tm_acc, BwdArgs a, int n_ktiles) {
+                        const __grid_constant__ CUtensorMap tm_acc, const __grid_constant__ CUtensorMap tm_dk,
+                        const __grid_constant__ CUtensorMap tm_dv, BwdArgs a, int n_ktiles) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -425,20 +424,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue: dK (scaled) from warps 0-3, dV from warps 4-7
         if (ok && n_it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.acc_done, 0, wd, 0xe2));
         tc_fence_after();
-        const MutView &ov = half == 0 ? a.dk : a.dv;
-        T *dstp = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss + (int64_t)hk * ov.sh;
         const float mul = half == 0 ? g.scale : 1.f;
         const uint32_t base = tmem + (half == 0 ? kTmDK : kTmDV) + lane_off;
+        // The K and V tiles are idle once every MMA has completed: stage the
+        // tile there (same 128B-swizzled layout as the loads) and write it
+        // with TMA stores, which drop rows past a dense tensor's end.  A THD
+        // tile that ends inside the tensor would spill into the next
+        // sequence, so it is written row by row instead.
+        if (!g.thd || nkeys == BK) {
+            uint8_t *stage = smem + (half == 0 ? kKOff : kVOff);
+            const uint32_t srow = smem_u32(stage) + j * 128;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t v[32];
-            if (n_it > 0) {
-                tmem_ld32(base + cc * 32, v);
-            } else {
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                if (n_it > 0) {
+                    tmem_ld32(base + cc * 32, v);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack2<T>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                // 16-byte chunks 4 cc .. 4 cc + 3 of the row: atom (chunk / 8),
+                // position (chunk % 8) ^ (row % 8) inside the atom's row
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c16 = cc * 4 + q;
+                    st_shared_v4(srow + (c16 / 8) * (BK * 128) + ((uint32_t)((c16 % 8) ^ (j & 7)) << 4), w[4 * q],
+                                 w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                }
             }
-            if (j < nkeys) store_row32<T>(dstp + cc * 32, v, mul);
+            fence_proxy_async_smem();
+            named_bar_sync(1 + half, 128);
+            if (warp % 4 == 0 && lane == 0) {
+                const CUtensorMap *m = half == 0 ? &tm_dk : &tm_dv;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) tma_store_4d(m, stage + c * BK * 128, c * 64, s.kv0 + n0, hk, cb);
+                bulk_commit();
+                bulk_wait0();  // before the CTA's shared memory goes away
+            }
+        } else {
+            const MutView &ov = half == 0 ? a.dk : a.dv;
+            T *dstp = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss + (int64_t)hk * ov.sh;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                if (n_it > 0) {
+                    tmem_ld32(base + cc * 32, v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (j < nkeys) store_row32<T>(dstp + cc * 32, v, mul);
+            }
         }
     } else if (warp >= kDrainWarp0) {
         // ----------------------------------- dQ^T drain (thread = head dim)
@@ -532,7 +572,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
     uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
     uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
-    auto strides = [&](const View &v, const uint64_t dims[4], uint64_t out[3]) {
+    auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
         const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
         for (int i = 0; i < 3; ++i)
             out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
@@ -541,17 +581,21 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
     const uint64_t acc_heads = g.thd ? (uint64_t)g.Hq : (uint64_t)g.B * g.Hq;
     cudaError_t e;
     if (max_lkv > 0) {  // (no key at all: dk, dv are empty and dq = 0)
-        uint64_t sq[3], sk[3], sv[3], sd[3];
+        uint64_t sq[3], sk[3], sv[3], sd[3], sgk[3], sgv[3];
         strides(a.q, dq, sq);
         strides(a.k, dk, sk);
         strides(a.v, dk, sv);
         strides(a.dout, dq, sd);
-        CUtensorMap tq, tk, tv, tdo, tacc;
+        strides(a.dk, dk, sgk);
+        strides(a.dv, dk, sgv);
+        CUtensorMap tq, tk, tv, tdo, tacc, tgk, tgv;
         if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BQ)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BK)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BK)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BQ)) != cudaSuccess) return e;
         if ((e = make_tmap_f32_acc(&tacc, a.dq_acc, D, acc_rows, acc_heads, 32, BQ)) != cudaSuccess) return e;
+        if ((e = make_tmap_16bit(&tgk, a.dk.ptr, dt, dk, sgk, BK)) != cudaSuccess) return e;
+        if ((e = make_tmap_16bit(&tgv, a.dv.ptr, dt, dk, sgv, BK)) != cudaSuccess) return e;
         auto kern = tc_bwd_fused_kernel<T>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
             cudaSuccess)
@@ -560,7 +604,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdFused);
-        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, a, n_ktiles);
+        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, tgk, tgv, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
