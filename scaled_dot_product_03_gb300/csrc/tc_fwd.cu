@@ -87,7 +87,8 @@ struct TileRange {
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, FwdArgs a, int n_mtiles) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a,
+                  int n_mtiles) {
     using C = FwdCfg<D>;
     constexpr int KS = C::kStages;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -348,27 +349,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool valid = r < tr[i].nrows;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        T *orow = (T *)a.o.ptr + (int64_t)b * a.o.sb + (int64_t)(s.q0 + row) * a.o.ss +
-                  (int64_t)h * a.o.sh;
+        if (!g.thd || tr[i].nrows == BM) {
+            // Stage O_i in its Q tile (idle once the tile's last S MMA has
+            // completed, and its load has landed: a tile without keys may
+            // still have it in flight) in the load's 128B-swizzled layout and
+            // write it with TMA stores, which drop rows past a dense tensor's
+            // end.  A THD tile ending inside the tensor is written row by row.
+            if (nb > 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, wd, 0x32))) ok = false;
+            uint8_t *stage = smem + C::kQOff + i * C::kTileBytes;
+            const uint32_t srow = smem_u32(stage) + r * 128;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t ov[32];
-            if (n_i > 0) {
-                tmem_ld32(tO + cc * 32, ov);
-            } else {
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t ov[32];
+                if (n_i > 0) {
+                    tmem_ld32(tO + cc * 32, ov);
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) ov[e] = 0u;
-            }
-            if (valid) {
-                uint4 pk[4];
-                uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
+                    for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                }
+                uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    pw[e] = pack2<T>(__uint_as_float(ov[2 * e]) * inv,
-                                     __uint_as_float(ov[2 * e + 1]) * inv);
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+                    w[e] = pack2<T>(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) dst[e] = pk[e];
+                for (int q = 0; q < 4; ++q) {
+                    const int c16 = cc * 4 + q;  // 16-byte chunk of the row: atom c16 / 8
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     srow + (c16 / 8) * (BM * 128) + ((uint32_t)((c16 % 8) ^ (r & 7)) << 4)),
+                                 "r"(w[4 * q]), "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3])
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + i, 128);
+            if (wq == 0 && lane == 0) {
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_store_4d(&tm_o, stage + c * BM * 128, c * 64, q_row + i * BM, h, qb);
+                bulk_commit();
+                bulk_wait0();  // before the CTA's shared memory goes away
+            }
+        } else {
+            T *orow = (T *)a.o.ptr + (int64_t)b * a.o.sb + (int64_t)(s.q0 + row) * a.o.ss +
+                      (int64_t)h * a.o.sh;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t ov[32];
+                if (n_i > 0) {
+                    tmem_ld32(tO + cc * 32, ov);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                }
+                if (valid) {
+                    uint4 pk[4];
+                    uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pw[e] = pack2<T>(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = pk[e];
+                }
             }
         }
         if (valid)
@@ -387,26 +429,28 @@ template <typename T, int D>
 cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t es = 2;
     // dims (d, rows, heads, batch); THD: rows = all tokens, one batch
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
     uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
     uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
     // byte strides of (rows, heads, batch); a size-1 dim may carry any stride
-    auto strides = [&](const View &v, const uint64_t dims[4], uint64_t out[3]) {
+    auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
         const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
         for (int i = 0; i < 3; ++i)
             out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
     };
-    uint64_t sq[3], sk[3], sv[3];
+    uint64_t sq[3], sk[3], sv[3], so[3];
     strides(a.q, dq, sq);
     strides(a.k, dk, sk);
     strides(a.v, dk, sv);
+    strides(a.o, dq, so);
     cudaError_t e;
     if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BM)) != cudaSuccess) return e;
     if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BN)) != cudaSuccess) return e;
     if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_16bit(&to, a.o.ptr, dt, dq, so, BM)) != cudaSuccess) return e;
     const int smem = FwdCfg<D>::kSmemBytes;
     auto kern = tc_fwd_kernel<T, D>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
@@ -417,7 +461,7 @@ cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
     prof_before(st, kProfFwd);
-    kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, a, n_mtiles);
+    kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, to, a, n_mtiles);
     prof_after(st);
     return cudaGetLastError();
 }
