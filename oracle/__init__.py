@@ -57,11 +57,13 @@ def _load():
                                             f64, i32, i32, P, P, P]
             lib.oracle_attn_fwd.restype = None
             lib.oracle_attn_bwd.argtypes = [i32, P, P, i32, i32, i32, P, P, P,
-                                            P, f64, i32, i32, P, P, P, P, P,
+                                            P, P, f64, i32, i32, P, P, P, P, P,
                                             P, P]
             lib.oracle_attn_bwd.restype = None
             lib.oracle_merge_lse.argtypes = [i64, i32, P, P, P, P, P, P]
             lib.oracle_merge_lse.restype = None
+            lib.oracle_merge_lse_bwd.argtypes = [i64, i32, P, P, P, P, P, P, P, P, P, P]
+            lib.oracle_merge_lse_bwd.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i32
             _lib = lib
@@ -113,8 +115,9 @@ def attn_fwd(q, k, v, cu_q, cu_kv, scale, window=(-1, -1), row_sel=None):
 
 
 def attn_bwd(q, k, v, dout, cu_q, cu_kv, scale, window=(-1, -1),
-             row_sel=None, key_sel=None, want_stats=False):
-    """Returns ``(dq, dk, dv)`` (plus ``(lse, r)`` with ``want_stats``)."""
+             row_sel=None, key_sel=None, want_stats=False, dlse=None):
+    """Returns ``(dq, dk, dv)`` (plus ``(lse, r)`` with ``want_stats``).
+    ``dlse`` ``[Tq, Hq]``: gradient with respect to the LSE output (None: 0)."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     cu_q = np.ascontiguousarray(cu_q, dtype=np.int64)
     cu_kv = np.ascontiguousarray(cu_kv, dtype=np.int64)
@@ -122,13 +125,16 @@ def attn_bwd(q, k, v, dout, cu_q, cu_kv, scale, window=(-1, -1),
     Tkv, Hkv, _ = k.shape
     assert dout.shape == q.shape and Hq % Hkv == 0
     rs, ks = _sel(row_sel, (Tq, Hq)), _sel(key_sel, (Tkv, Hkv))
+    if dlse is not None:
+        dlse = _f64(dlse)
+        assert dlse.shape == (Tq, Hq)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     lse = np.full((Tq, Hq), np.nan) if want_stats else None
     r = np.full((Tq, Hq), np.nan) if want_stats else None
     _load().oracle_attn_bwd(len(cu_q) - 1, _ptr(cu_q), _ptr(cu_kv), Hq, Hkv, D,
-                            _ptr(q), _ptr(k), _ptr(v), _ptr(dout), float(scale),
+                            _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dlse), float(scale),
                             int(window[0]), int(window[1]), _ptr(rs), _ptr(ks),
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(lse), _ptr(r))
     if want_stats:
@@ -149,3 +155,23 @@ def merge_lse(o1, lse1, o2, lse2):
     _load().oracle_merge_lse(n, D, _ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2),
                              _ptr(o), _ptr(lse))
     return o, lse
+
+
+def merge_lse_bwd(o1, lse1, o2, lse2, dout, dlse=None):
+    """Backward of :func:`merge_lse`: ``(do1, dlse1, do2, dlse2)`` for the
+    gradients ``dout`` of the merged o and ``dlse`` of the merged lse."""
+    o1, o2, dout = _f64(o1), _f64(o2), _f64(dout)
+    lse1, lse2 = _f64(lse1), _f64(lse2)
+    shape = o1.shape
+    D = shape[-1]
+    n = int(np.prod(shape[:-1]))
+    assert o2.shape == shape == dout.shape and lse1.shape == shape[:-1] == lse2.shape
+    if dlse is not None:
+        dlse = _f64(dlse)
+        assert dlse.shape == shape[:-1]
+    do1, do2 = np.empty(shape), np.empty(shape)
+    dl1, dl2 = np.empty(shape[:-1]), np.empty(shape[:-1])
+    _load().oracle_merge_lse_bwd(n, D, _ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2),
+                                 _ptr(dout), _ptr(dlse), _ptr(do1), _ptr(dl1),
+                                 _ptr(do2), _ptr(dl2))
+    return do1, dl1, do2, dl2

@@ -38,10 +38,13 @@
  *   q, o, dq : [Tq][Hq][D]      k, v, dk, dv : [Tkv][Hkv][D]
  *   lse, delta : [Tq][Hq]
  *
- * Backward (gradient of sum(dO * O) as in the repro's out.sum().backward()):
+ * Backward (gradient of sum(dO * O) as in the repro's out.sum().backward(),
+ * plus sum(dLSE * LSE) when an LSE gradient is given: the flex-attention
+ * issue returns the LSE and merges through it, so a loss can reach the
+ * scores through LSE as well as through O; d LSE_i / d s_ij = p_ij):
  *   dP_ij = <dO_i, v_j>
  *   r_i   = sum_j p_ij dP_ij          (the definitional softmax row term)
- *   dS_ij = p_ij (dP_ij - r_i)
+ *   dS_ij = p_ij (dP_ij - r_i + dLSE_i)
  *   dq_i  = scale * sum_j dS_ij k_j
  *   dk_j  = scale * sum_{h in group} sum_i dS_ij q_i
  *   dv_j  = sum_{h in group} sum_i p_ij dO_i
@@ -50,6 +53,13 @@
  * partial results are weighted by exp(lse - max) and renormalised.  When
  * both sides are -inf (no visible key on either side) the merged row is
  * o = 0, lse = -inf instead of the NaN the formula would give.
+ *
+ * Merge backward: the derivative of that formula.  With w_k = e_k / (e1 + e2),
+ * o = w1 o1 + w2 o2 and lse = m + log(e1 + e2):
+ *   d o / d o_k = w_k,   d o / d lse_k = w_k (o_k - o),   d lse / d lse_k = w_k
+ * so for upstream gradients dO, dLSE of the merged row:
+ *   dO_k = w_k dO,   dLSE_k = w_k (<dO, o_k - o> + dLSE)
+ * (both zero for a side whose lse is -inf).
  */
 #include <math.h>
 #include <stdint.h>
@@ -141,16 +151,18 @@ void oracle_attn_fwd(int nseq, const int64_t *cu_q, const int64_t *cu_kv,
     }
 }
 
-/* Backward.  row_sel (optional, [Tq][Hq]) selects the dq rows to compute,
- * key_sel (optional, [Tkv][Hkv]) the dk/dv rows; unselected outputs are left
- * untouched.  lse_out and r_out (optional, [Tq][Hq]) receive LSE_i and the
- * row term r_i of every row that some selected output depends on. */
+/* Backward.  dlse (optional, [Tq][Hq]) is the gradient of the loss with
+ * respect to LSE (NULL: zero).  row_sel (optional, [Tq][Hq]) selects the dq
+ * rows to compute, key_sel (optional, [Tkv][Hkv]) the dk/dv rows;
+ * unselected outputs are left untouched.  lse_out and r_out (optional,
+ * [Tq][Hq]) receive LSE_i and the row term r_i of every row that some
+ * selected output depends on. */
 void oracle_attn_bwd(int nseq, const int64_t *cu_q, const int64_t *cu_kv,
                      int Hq, int Hkv, int D, const double *q, const double *k,
-                     const double *v, const double *dout, double scale, int wl,
-                     int wr, const uint8_t *row_sel, const uint8_t *key_sel,
-                     double *dq, double *dk, double *dv, double *lse_out,
-                     double *r_out) {
+                     const double *v, const double *dout, const double *dlse,
+                     double scale, int wl, int wr, const uint8_t *row_sel,
+                     const uint8_t *key_sel, double *dq, double *dk, double *dv,
+                     double *lse_out, double *r_out) {
     const int G = Hq / Hkv;
     const int64_t Tq = cu_q[nseq], Tkv = cu_kv[nseq];
     const int64_t Lmax = max_len(nseq, cu_kv);
@@ -213,7 +225,8 @@ void oracle_attn_bwd(int nseq, const int64_t *cu_q, const int64_t *cu_kv,
             const double *krow = k + ((kv0 + j) * Hkv + hk) * D;
             const double *vrow = v + ((kv0 + j) * Hkv + hk) * D;
             const double p = exp(scale * dot(q + r * D, krow, D) - L[r]);
-            const double dS = p * (dot(dout + r * D, vrow, D) - R[r]);
+            const double g = dlse ? dlse[r] : 0.0;
+            const double dS = p * (dot(dout + r * D, vrow, D) - R[r] + g);
             for (int d = 0; d < D; ++d) dqrow[d] += scale * dS * krow[d];
         }
     }
@@ -236,7 +249,8 @@ void oracle_attn_bwd(int nseq, const int64_t *cu_q, const int64_t *cu_kv,
                 const int64_t i = t - cu_q[b], r = t * Hq + h;
                 if (!visible(i, j, len_kv, wl, wr)) continue;
                 const double p = exp(scale * dot(q + r * D, krow, D) - L[r]);
-                const double dS = p * (dot(dout + r * D, vrow, D) - R[r]);
+                const double g = dlse ? dlse[r] : 0.0;
+                const double dS = p * (dot(dout + r * D, vrow, D) - R[r] + g);
                 for (int d = 0; d < D; ++d) {
                     dkrow[d] += scale * dS * q[r * D + d];
                     dvrow[d] += p * dout[r * D + d];
@@ -266,6 +280,36 @@ void oracle_merge_lse(int64_t n, int D, const double *o1, const double *lse1,
         for (int d = 0; d < D; ++d)
             o[r * D + d] = (o1[r * D + d] * e1 + o2[r * D + d] * e2) / (e1 + e2);
         lse[r] = mx + log(e1 + e2);
+    }
+}
+
+/* Backward of the LSE merge.  dout : [n][D] gradient of the merged o;
+ * dlse (optional) : [n] gradient of the merged lse; outputs do1, do2 : [n][D]
+ * and dlse1, dlse2 : [n]. */
+void oracle_merge_lse_bwd(int64_t n, int D, const double *o1, const double *lse1,
+                          const double *o2, const double *lse2,
+                          const double *dout, const double *dlse, double *do1,
+                          double *dlse1, double *do2, double *dlse2) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        const double mx = lse1[r] > lse2[r] ? lse1[r] : lse2[r];
+        double w1 = 0.0, w2 = 0.0;
+        if (mx != -INFINITY) {
+            const double e1 = exp(lse1[r] - mx), e2 = exp(lse2[r] - mx);
+            w1 = e1 / (e1 + e2);
+            w2 = e2 / (e1 + e2);
+        }
+        double g1 = 0.0, g2 = 0.0;  /* <dO, o_k - o> */
+        for (int d = 0; d < D; ++d) {
+            const double o = w1 * o1[r * D + d] + w2 * o2[r * D + d];
+            g1 += dout[r * D + d] * (o1[r * D + d] - o);
+            g2 += dout[r * D + d] * (o2[r * D + d] - o);
+            do1[r * D + d] = w1 * dout[r * D + d];
+            do2[r * D + d] = w2 * dout[r * D + d];
+        }
+        const double g = dlse ? dlse[r] : 0.0;
+        dlse1[r] = w1 * (g1 + g);
+        dlse2[r] = w2 * (g2 + g);
     }
 }
 

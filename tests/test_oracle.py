@@ -249,6 +249,124 @@ def test_merge_with_empty_sides():
     assert np.all(o[3] == 0) and np.isneginf(lse[3])
 
 
+# -- 6b. gradient through the LSE output and through the merge ---------------
+# The flex-attention issue returns the LSE and combines two partial results
+# through it (merge_attn); training such a split needs the gradient of a loss
+# that reaches the scores through LSE as well as O, and the backward of the
+# merge.
+
+def _fd(f, arrays, h=1e-6):
+    """Central differences of f(*arrays) with respect to every element."""
+    out = []
+    for n in range(len(arrays)):
+        g = np.zeros_like(arrays[n])
+        for idx in np.ndindex(arrays[n].shape):
+            xp = [a.copy() for a in arrays]
+            xm = [a.copy() for a in arrays]
+            xp[n][idx] += h
+            xm[n][idx] -= h
+            g[idx] = (f(*xp) - f(*xm)) / (2 * h)
+        out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("window", [(-1, -1), (-1, 0), (1, 1)])
+def test_lse_gradient_matches_central_differences(window):
+    q, k, v, cq, ck = _dense(1, 5, 5, 2, 1, 4, seed=61)
+    dout = _rand(q.shape, 62)
+    dlse = _rand(q.shape[:2], 63)
+    scale = 0.6
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dout, cq, ck, scale, window, dlse=dlse)
+
+    def f(q_, k_, v_):
+        o, lse = oracle.attn_fwd(q_, k_, v_, cq, ck, scale, window)
+        return float(np.sum(o * dout) + np.sum(lse * dlse))
+
+    for name, fd, g in zip("qkv", _fd(f, [q, k, v]), (dq, dk, dv)):
+        err = np.abs(fd - g).max() / max(1.0, np.abs(g).max())
+        assert err < 1e-6, (name, err)
+
+
+def test_lse_gradient_matches_torch_autograd():
+    """The same loss written with torch's softmax and logsumexp (float64,
+    autograd), grouped heads and a causal mask."""
+    B, S, Hq, Hkv, D, scale = 1, 9, 4, 2, 8, 0.45
+    q, k, v, cq, ck = _dense(B, S, S, Hq, Hkv, D, seed=64)
+    dout, dlse = _rand(q.shape, 65), _rand(q.shape[:2], 66)
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    G = Hq // Hkv
+    kk, vv = tk.repeat_interleave(G, dim=1), tv.repeat_interleave(G, dim=1)   # [S, Hq, D]
+    s = scale * torch.einsum("ihd,jhd->hij", tq, kk)
+    mask = torch.ones(S, S, dtype=torch.bool).tril()
+    s = s.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)                       # [Hq, S]
+    o = torch.einsum("hij,jhd->ihd", torch.softmax(s, dim=-1), vv)
+    loss = (o * torch.tensor(dout)).sum() + (lse.T * torch.tensor(dlse)).sum()
+    loss.backward()
+    dq, dk, dv = oracle.attn_bwd(q, k, v, dout, cq, ck, scale, (-1, 0), dlse=dlse)
+    for a, t in ((dq, tq), (dk, tk), (dv, tv)):
+        np.testing.assert_allclose(a, t.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_merge_backward_matches_central_differences():
+    n, D = 6, 3
+    o1, o2 = _rand((n, D), 71), _rand((n, D), 72)
+    l1, l2 = _rand((n,), 73), _rand((n,), 74) * 2.0
+    dout, dlse = _rand((n, D), 75), _rand((n,), 76)
+    do1, dl1, do2, dl2 = oracle.merge_lse_bwd(o1, l1, o2, l2, dout, dlse)
+
+    def f(a1, b1, a2, b2):
+        o, lse = oracle.merge_lse(a1, b1, a2, b2)
+        return float(np.sum(o * dout) + np.sum(lse * dlse))
+
+    for name, fd, g in zip(("o1", "lse1", "o2", "lse2"), _fd(f, [o1, l1, o2, l2]),
+                           (do1, dl1, do2, dl2)):
+        np.testing.assert_allclose(g, fd, rtol=1e-7, atol=1e-8, err_msg=name)
+
+
+def test_merge_backward_with_empty_sides():
+    """A side without keys gets no gradient; the other side then is the
+    merged row itself, so it receives dO unchanged and the LSE gradient as
+    is; both sides empty: nothing anywhere."""
+    o1, o2, dout = _rand((3, 4), 81), _rand((3, 4), 82), _rand((3, 4), 83)
+    l1 = np.array([-np.inf, 0.7, -np.inf])
+    l2 = np.array([1.1, -np.inf, -np.inf])
+    dlse = np.array([0.3, -0.8, 0.5])
+    do1, dl1, do2, dl2 = oracle.merge_lse_bwd(o1, l1, o2, l2, dout, dlse)
+    assert np.all(do1[0] == 0) and dl1[0] == 0
+    np.testing.assert_allclose(do2[0], dout[0])
+    np.testing.assert_allclose(dl2[0], dlse[0])
+    assert np.all(do2[1] == 0) and dl2[1] == 0
+    np.testing.assert_allclose(do1[1], dout[1])
+    np.testing.assert_allclose(dl1[1], dlse[1])
+    assert np.all(do1[2] == 0) and np.all(do2[2] == 0) and dl1[2] == 0 and dl2[2] == 0
+
+
+def test_local_global_split_trains_like_causal():
+    """Page 3's v1 split trained end to end: the gradients of a loss on the
+    merged O and LSE, taken back through merge_attn and through both partial
+    attentions (each with its LSE gradient), equal those of full causal
+    attention."""
+    S, H, D, band, scale = 40, 3, 8, 6, 0.4
+    q, k, v, cq, ck = _dense(1, S, S, H, H, D, seed=91)
+    dout, dlse = _rand(q.shape, 92), _rand(q.shape[:2], 93)
+    sh = band + 1
+    cg = np.array([0, S - sh])
+    o_loc, lse_loc = oracle.attn_fwd(q, k, v, cq, ck, scale, (band, 0))
+    o_glb, lse_glb = oracle.attn_fwd(q[sh:], k, v, cg, ck, scale, (-1, 0))
+    do_lt, dl_lt, do_g, dl_g = oracle.merge_lse_bwd(o_loc[sh:], lse_loc[sh:], o_glb, lse_glb,
+                                                    dout[sh:], dlse[sh:])
+    do_l = np.concatenate([dout[:sh], do_lt])
+    dl_l = np.concatenate([dlse[:sh], dl_lt])
+    dq_l, dk_l, dv_l = oracle.attn_bwd(q, k, v, do_l, cq, ck, scale, (band, 0), dlse=dl_l)
+    dq_g, dk_g, dv_g = oracle.attn_bwd(q[sh:], k, v, do_g, cg, ck, scale, (-1, 0), dlse=dl_g)
+    dq = dq_l.copy()
+    dq[sh:] += dq_g
+    dq_f, dk_f, dv_f = oracle.attn_bwd(q, k, v, dout, cq, ck, scale, (-1, 0), dlse=dlse)
+    for a, b in ((dq, dq_f), (dk_l + dk_g, dk_f), (dv_l + dv_g, dv_f)):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
+
+
 # -- 7. identities of the softmax gradient -----------------------------------
 
 def test_row_term_equals_dout_dot_out():
