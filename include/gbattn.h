@@ -166,6 +166,23 @@ GBATTN_API attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor
                      attn_stream_t stream);
 
 /*
+ * attn_bwd for a loss that also depends on the forward's LSE output
+ * ("Significant Accuracy Difference between Compiled and Eager Flex
+ * Attention": flex_attention returns the LSE and merge_attn combines two
+ * partial attentions through it, so training that split sends a gradient
+ * into each part's LSE).  dlse: gradient of the loss with respect to lse,
+ * fp32 in the LSE layout (NULL: zero, which is attn_bwd).  Since
+ * d LSE_i / d s_ij = P_ij, it adds P_ij dLSE_i to dS_ij:
+ *   dS_ij = P_ij (<dO_i, v_j> - <dO_i, O_i> + dLSE_i).
+ * Everything else (arguments, workspace, determinism) is as for attn_bwd.
+ */
+GBATTN_API attn_status attn_bwd_dlse(const attn_params *p, attn_tensor q, attn_tensor k,
+                          attn_tensor v, attn_tensor o, attn_tensor dout,
+                          const float *lse, const float *dlse, attn_tensor dq,
+                          attn_tensor dk, attn_tensor dv, void *workspace,
+                          size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Merge two partial attentions of the same queries over disjoint key sets
  * (merge_attn in "Significant Accuracy Difference between Compiled and Eager
  * Flex Attention"):
@@ -184,6 +201,24 @@ GBATTN_API attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int
                            attn_tensor o1, const float *lse1, attn_tensor o2,
                            const float *lse2, attn_tensor o_out,
                            float *lse_out, attn_stream_t stream);
+
+/*
+ * Backward of attn_merge_lse: given the partial results (o1, lse1), (o2,
+ * lse2) that were merged and the gradients dout of the merged o and dlse of
+ * the merged lse (NULL: zero), writes
+ *   do_k   = w_k dout,
+ *   dlse_k = w_k (<dout, o_k - o> + dlse),   w_k = exp(lse_k - lse),
+ * the derivative of the merge formula (o = w1 o1 + w2 o2 recomputed in
+ * fp32).  A side whose lse is -inf gets zeros.  Layouts and limits as for
+ * attn_merge_lse; dout, do1, do2 are views of element type dtype, dlse1 and
+ * dlse2 fp32 [B, H, S].  No output may overlap an input or another output;
+ * o1 and o2 must be finite.
+ */
+GBATTN_API attn_status attn_merge_lse_bwd(attn_dtype dtype, int B, int S, int H, int D,
+                               attn_tensor o1, const float *lse1, attn_tensor o2,
+                               const float *lse2, attn_tensor dout, const float *dlse,
+                               attn_tensor do1, float *dlse1, attn_tensor do2,
+                               float *dlse2, attn_stream_t stream);
 
 /*
  * Per-launch timing, for benchmarks and profilers.  After
@@ -205,7 +240,8 @@ enum {
     ATTN_KERNEL_SIMT_BWD_DQ = 6,    /* fp32 dQ */
     ATTN_KERNEL_SIMT_BWD_DKDV = 7,  /* fp32 dK, dV */
     ATTN_KERNEL_BWD_FUSED = 8,      /* tensor-core single-pass dK, dV, dQ share */
-    ATTN_KERNEL_BWD_DQ_CONVERT = 9  /* fp32 dq accumulator -> dq */
+    ATTN_KERNEL_BWD_DQ_CONVERT = 9, /* fp32 dq accumulator -> dq */
+    ATTN_KERNEL_MERGE_BWD = 10      /* backward of the LSE merge */
 };
 GBATTN_API attn_status attn_profile_begin(int max_launches);
 GBATTN_API int attn_profile_read(float *ms, int *kind, int capacity);

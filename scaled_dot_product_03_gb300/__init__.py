@@ -122,10 +122,11 @@ def attn_bwd_workspace_size(q, k, **kw) -> int:
 
 def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens_q=None,
              cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None, dk=None,
-             dv=None, workspace=None, deterministic=False
+             dv=None, workspace=None, deterministic=False, dlse=None
              ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """Backward attention: ``(dq, dk, dv)`` for upstream gradient ``dout``,
-    recomputing P from q, k and the forward's ``lse``.  ``workspace`` (uint8
+    """Backward attention: ``(dq, dk, dv)`` for upstream gradient ``dout``
+    (and ``dlse``, the gradient with respect to the forward's LSE output,
+    fp32 in its layout; None: zero), recomputing P from q, k and ``lse``.  ``workspace`` (uint8
     device tensor of at least :func:`attn_bwd_workspace_size` bytes, with the
     same ``deterministic``) is allocated when not given.  ``deterministic``
     selects the bitwise-reproducible two-kernel backward instead of the
@@ -145,11 +146,18 @@ def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens
     need = int(lib.attn_bwd_workspace_size(p))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    _lib.check(lib.attn_bwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
-                            _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
-                            _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd),
-                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                            _stream(q)))
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    if dlse is None:
+        _lib.check(lib.attn_bwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                                _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
+                                _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd), *ws,
+                                _stream(q)))
+    else:
+        assert dlse.dtype == torch.float32 and dlse.is_contiguous() and dlse.shape == lse.shape
+        _lib.check(lib.attn_bwd_dlse(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                                     _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
+                                     dlse.data_ptr(), _tensor(dq, thd), _tensor(dk, thd),
+                                     _tensor(dv, thd), *ws, _stream(q)))
     return dq, dk, dv
 
 
@@ -206,6 +214,37 @@ def attn_merge_lse(o1, lse1, o2, lse2, *, out=None, lse_out=None
                                   lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
                                   _tensor(views[2], False), lse_out.data_ptr(), _stream(o1)))
     return out, lse_out
+
+
+def attn_merge_lse_bwd(o1, lse1, o2, lse2, dout, dlse=None, *, do1=None, dlse1=None, do2=None,
+                       dlse2=None):
+    """Backward of :func:`attn_merge_lse`: ``(do1, dlse1, do2, dlse2)`` for
+    the gradients ``dout`` of the merged o and ``dlse`` of the merged lse
+    (None: zero).  Shapes as for :func:`attn_merge_lse`."""
+    do1 = torch.empty(o1.shape, dtype=o1.dtype, device=o1.device) if do1 is None else do1
+    do2 = torch.empty(o2.shape, dtype=o2.dtype, device=o2.device) if do2 is None else do2
+    dlse1 = torch.empty_like(lse1) if dlse1 is None else dlse1
+    dlse2 = torch.empty_like(lse2) if dlse2 is None else dlse2
+    if o1.dim() == 3:
+        T, H, D = o1.shape
+        B, S = 1, T
+        views = [x.unsqueeze(0) for x in (o1, o2, dout, do1, do2)]
+    else:
+        B, S, H, D = o1.shape
+        views = [o1, o2, dout, do1, do2]
+    lses = [lse1, lse2, dlse1, dlse2] + ([] if dlse is None else [dlse])
+    for l in lses:
+        assert l.dtype == torch.float32 and l.is_contiguous() and l.numel() == B * H * S
+    if o1.dtype not in _DTYPES:
+        raise TypeError("unsupported dtype %s" % o1.dtype)
+    lib = _lib.load()
+    _lib.check(lib.attn_merge_lse_bwd(_DTYPES[o1.dtype], B, S, H, D, _tensor(views[0], False),
+                                      lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
+                                      _tensor(views[2], False),
+                                      None if dlse is None else dlse.data_ptr(),
+                                      _tensor(views[3], False), dlse1.data_ptr(),
+                                      _tensor(views[4], False), dlse2.data_ptr(), _stream(o1)))
+    return do1, dlse1, do2, dlse2
 
 
 def profile_begin(max_launches: int) -> None:

@@ -285,10 +285,14 @@ size_t attn_bwd_workspace_size(const attn_params *p) {
     return ws_layout(p).total;
 }
 
-attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_tensor v,
-                     attn_tensor o, attn_tensor dout, const float *lse, attn_tensor dq,
-                     attn_tensor dk, attn_tensor dv, void *workspace, size_t workspace_bytes,
-                     attn_stream_t stream) {
+}  // extern "C"
+
+namespace gbattn {
+namespace {
+
+attn_status bwd_impl(const attn_params *p, attn_tensor q, attn_tensor k, attn_tensor v, attn_tensor o,
+                     attn_tensor dout, const float *lse, const float *dlse, attn_tensor dq, attn_tensor dk,
+                     attn_tensor dv, void *workspace, size_t workspace_bytes, attn_stream_t stream) {
     t_error.clear();
     attn_status st = check_params(p);
     if (st != ATTN_OK) return st;
@@ -314,6 +318,7 @@ attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     a.o = view_of(p, o);
     a.dout = view_of(p, dout);
     a.lse = lse;
+    a.dlse = dlse;
     a.dq = mview_of(p, dq);
     a.dk = mview_of(p, dk);
     a.dv = mview_of(p, dv);
@@ -332,6 +337,25 @@ attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
         e = launch_simt_bwd(p->dtype, a, max_lq(p), max_lkv(p), s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
     return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+extern "C" {
+
+attn_status attn_bwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_tensor v,
+                     attn_tensor o, attn_tensor dout, const float *lse, attn_tensor dq,
+                     attn_tensor dk, attn_tensor dv, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream) {
+    return bwd_impl(p, q, k, v, o, dout, lse, nullptr, dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_dlse(const attn_params *p, attn_tensor q, attn_tensor k, attn_tensor v,
+                          attn_tensor o, attn_tensor dout, const float *lse, const float *dlse,
+                          attn_tensor dq, attn_tensor dk, attn_tensor dv, void *workspace,
+                          size_t workspace_bytes, attn_stream_t stream) {
+    return bwd_impl(p, q, k, v, o, dout, lse, dlse, dq, dk, dv, workspace, workspace_bytes, stream);
 }
 
 attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int D, attn_tensor o1,
@@ -365,6 +389,45 @@ attn_status attn_merge_lse(attn_dtype dtype, int B, int S, int H, int D, attn_te
     a.lse_out = lse_out;
     cudaError_t e = launch_merge(dtype, a, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "attn_merge_lse launch");
+    return ATTN_OK;
+}
+
+attn_status attn_merge_lse_bwd(attn_dtype dtype, int B, int S, int H, int D, attn_tensor o1,
+                               const float *lse1, attn_tensor o2, const float *lse2, attn_tensor dout,
+                               const float *dlse, attn_tensor do1, float *dlse1, attn_tensor do2,
+                               float *dlse2, attn_stream_t stream) {
+    t_error.clear();
+    if (!dtype_ok(dtype)) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B < 0 || S < 0 || H < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size");
+    if (D < 1 || D > 256) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not in 1..256", D);
+    if ((int64_t)B * S * H == 0) return ATTN_OK;
+    const attn_tensor *ts[5] = {&o1, &o2, &dout, &do1, &do2};
+    const char *names[5] = {"o1", "o2", "dout", "do1", "do2"};
+    for (int i = 0; i < 5; ++i) {
+        if (!ts[i]->ptr) return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", names[i]);
+        if (ts[i]->stride[3] != 1)
+            return fail(ATTN_ERR_UNSUPPORTED, "%s: innermost stride must be 1", names[i]);
+        if ((uintptr_t)ts[i]->ptr % elt_size(dtype))
+            return fail(ATTN_ERR_UNSUPPORTED, "%s: misaligned pointer", names[i]);
+    }
+    if (!lse1 || !lse2 || !dlse1 || !dlse2) return fail(ATTN_ERR_INVALID_ARG, "lse: NULL pointer");
+    MergeBwdArgs a;
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.D = D;
+    a.o1 = View{o1.ptr, o1.stride[0], o1.stride[1], o1.stride[2]};
+    a.o2 = View{o2.ptr, o2.stride[0], o2.stride[1], o2.stride[2]};
+    a.dout = View{dout.ptr, dout.stride[0], dout.stride[1], dout.stride[2]};
+    a.do1 = MutView{do1.ptr, do1.stride[0], do1.stride[1], do1.stride[2]};
+    a.do2 = MutView{do2.ptr, do2.stride[0], do2.stride[1], do2.stride[2]};
+    a.lse1 = lse1;
+    a.lse2 = lse2;
+    a.dlse = dlse;
+    a.dlse1 = dlse1;
+    a.dlse2 = dlse2;
+    cudaError_t e = launch_merge_bwd(dtype, a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_merge_lse_bwd launch");
     return ATTN_OK;
 }
 

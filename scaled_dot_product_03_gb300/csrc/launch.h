@@ -19,7 +19,8 @@ struct BwdArgs {
     View q, k, v, o, dout;
     const float *lse;
     MutView dq, dk, dv;
-    float *delta;         // workspace: row terms <dO_i, O_i>, laid out like LSE
+    const float *dlse;    // optional gradient of the loss w.r.t. LSE (LSE layout)
+    float *delta;         // workspace: row terms <dO_i, O_i> - dLSE_i, laid out like LSE
     float *dq_acc;        // fp32 dq accumulator laid out like LSE with D columns
                           // per row, cleared by the preprocess kernel; null when
                           // the backward does not use one
@@ -41,5 +42,14 @@ cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv
                             cudaStream_t st);
 cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStream_t st);
 cudaError_t launch_merge(int dtype, const MergeArgs &a, cudaStream_t st);
+
+struct MergeBwdArgs {
+    int B, S, H, D;
+    View o1, o2, dout;
+    MutView do1, do2;
+    const float *lse1, *lse2, *dlse;  // dlse may be null
+    float *dlse1, *dlse2;
+};
+cudaError_t launch_merge_bwd(int dtype, const MergeBwdArgs &a, cudaStream_t st);
 
 }  // namespace gbattn

@@ -19,6 +19,7 @@ enum ProfKind {
     kProfSimtBwdDkDv = 7,
     kProfBwdFused = 8,
     kProfBwdDqConvert = 9,
+    kProfMergeBwd = 10,
 };
 
 void prof_before(cudaStream_t st, int kind);

@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward preprocess: delta = <dO, O> per (row, head).  A group of up to 32
+// Backward preprocess: delta = <dO, O> - dLSE per (row, head) (dLSE = 0 when
+// no LSE gradient is given).  A group of up to 32
 // lanes (power of two) covers one (row, head), each lane VEC elements at a
 // time.  Also clears the fp32 dq accumulator (laid out like LSE, D floats per
 // row) when the backward uses one.
@@ -162,7 +163,9 @@ __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
             }
         }
         for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (active && c0 == 0) a.delta[idx] = acc;
+        // a gradient reaching LSE adds P_ij dLSE_i to dS_ij, i.e. lowers the
+        // row term by dLSE_i
+        if (active && c0 == 0) a.delta[idx] = a.dlse ? acc - a.dlse[idx] : acc;
     }
 }
 

@@ -134,6 +134,29 @@ def test_workspace_size(lib):
     assert lib.attn_bwd_workspace_size(ctypes.byref(pf)) == 0
 
 
+def test_lse_gradient_backward_rejects_like_attn_bwd(lib):
+    """attn_bwd_dlse validates exactly as attn_bwd (nothing is launched)."""
+    t = _t()
+    for kw, status in ((dict(deterministic=2), _lib.ATTN_ERR_INVALID_ARG),
+                       (dict(D=96), _lib.ATTN_ERR_UNSUPPORTED)):
+        p = _params(**kw)
+        st = lib.attn_bwd_dlse(ctypes.byref(p), t, t, t, t, t, 4096, 4096, t, t, t, 4096, 1 << 20,
+                               None)
+        assert st == status, lib.attn_last_error_string()
+    p = _params()
+    st = lib.attn_bwd_dlse(ctypes.byref(p), t, t, t, t, t, None, 4096, t, t, t, 4096, 1 << 20, None)
+    assert st == _lib.ATTN_ERR_INVALID_ARG  # lse missing
+
+
+def test_merge_backward_rejects_bad_args(lib):
+    t, z = _t(), _t(ptr=0)
+    args = lambda dt, B, D, do1=t: (dt, B, 4, 2, D, t, 4096, t, 4096, t, None, do1, 4096, t, 4096, None)
+    assert lib.attn_merge_lse_bwd(*args(9, 1, 64)) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_merge_lse_bwd(*args(1, 1, 300)) == _lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_merge_lse_bwd(*args(1, 1, 64, do1=z)) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_merge_lse_bwd(*args(1, 0, 64)) == _lib.ATTN_OK  # empty: nothing to do
+
+
 def test_merge_rejects_bad_args(lib):
     t = _t()
     assert lib.attn_merge_lse(9, 1, 1, 1, 64, t, 4096, t, 4096, t, 4096, None) == \
