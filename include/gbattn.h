@@ -39,7 +39,15 @@
  *     for cuDNN FusedAttention + THD + CP", the thd branch): element
  *     (t, h, d) lives at ptr + t*stride[1] + h*stride[2] + d*stride[3]
  *     (stride[0] is ignored); sequence b owns token rows
- *     [cu_seqlens[b], cu_seqlens[b+1]).
+ *     [cu_seqlens[b], cu_seqlens[b+1]).  With cu_seqlens_*_padded (the
+ *     thread's cu_seqlens_q_padded / cu_seqlens_kv_padded, used where each
+ *     sequence is padded, e.g. to a multiple of 2 x the context-parallel
+ *     size) sequence b instead owns rows [padded[b], padded[b] + L_b) with
+ *     L_b = cu_seqlens[b+1] - cu_seqlens[b] (padded[b] + L_b <= padded[b+1]
+ *     is the caller's to ensure); rows in the gaps are never written and
+ *     the LSE keeps the buffer's row numbering.  Gap rows must hold finite
+ *     values: a tile that runs past a sequence multiplies them by exact
+ *     zero weights.
  * The innermost stride (d) must be 1.  For 16-bit types every other stride
  * and the base pointer must be 16-byte aligned (a tensor-memory-accelerator
  * requirement); otherwise the call fails with ATTN_ERR_UNSUPPORTED rather
@@ -116,6 +124,9 @@ typedef struct {
     int window_right;    /* -1 = unbounded; (-1, 0) = causal */
     int deterministic;   /* backward only (see attn_bwd): 0 = single pass with
                             an fp32 dq accumulator, 1 = bitwise reproducible */
+    const int32_t *cu_seqlens_q_padded;  /* THD only, optional (NULL: none): */
+    const int32_t *cu_seqlens_kv_padded; /* device, B + 1 first rows of the
+                            sequences in a padded buffer (see Layouts) */
 } attn_params;
 
 /*

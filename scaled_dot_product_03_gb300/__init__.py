@@ -55,8 +55,11 @@ def _tensor(t: Optional[torch.Tensor], thd: bool) -> "_lib.AttnTensor":
 
 
 def params_for(q, k, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seqlens_kv=None,
-               max_seqlen_q=None, max_seqlen_kv=None, deterministic=False) -> "_lib.AttnParams":
-    """The ``attn_params`` struct describing q (and k, v) views."""
+               max_seqlen_q=None, max_seqlen_kv=None, deterministic=False,
+               cu_seqlens_q_padded=None, cu_seqlens_kv_padded=None) -> "_lib.AttnParams":
+    """The ``attn_params`` struct describing q (and k, v) views.  THD
+    ``cu_seqlens_*_padded`` (int32, device): first row of each sequence in a
+    padded buffer."""
     p = _lib.AttnParams()
     p.deterministic = 1 if deterministic else 0
     if q.dtype not in _DTYPES:
@@ -76,6 +79,12 @@ def params_for(q, k, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seqle
         p.Skv, p.Hkv = k.shape[0], k.shape[1]
         p.cu_seqlens_q = cu_seqlens_q.data_ptr()
         p.cu_seqlens_kv = cu_seqlens_kv.data_ptr()
+        if cu_seqlens_q_padded is not None:
+            p.cu_seqlens_q_padded = cu_seqlens_q_padded.data_ptr()
+            if cu_seqlens_kv_padded is None:
+                cu_seqlens_kv_padded = cu_seqlens_q_padded
+        if cu_seqlens_kv_padded is not None:
+            p.cu_seqlens_kv_padded = cu_seqlens_kv_padded.data_ptr()
         if max_seqlen_q is None:  # needs a device->host read of cu_seqlens
             max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max()) if p.B else 0
         if max_seqlen_kv is None:
@@ -95,7 +104,8 @@ def _lse_shape(p):
 
 
 def attn_fwd(q, k, v, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seqlens_kv=None,
-             max_seqlen_q=None, max_seqlen_kv=None, out=None, lse=None
+             max_seqlen_q=None, max_seqlen_kv=None, out=None, lse=None,
+             cu_seqlens_q_padded=None, cu_seqlens_kv_padded=None
              ) -> Tuple[torch.Tensor, torch.Tensor]:
     """Forward attention.  Dense: q ``[B, Sq, Hq, D]``, k/v ``[B, Skv, Hkv, D]``
     (any strides, d contiguous).  THD (``cu_seqlens_q`` given): q ``[Tq, Hq, D]``,
@@ -103,7 +113,8 @@ def attn_fwd(q, k, v, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seql
     causal.  Returns ``(o, lse)`` with lse fp32 ``[B, Hq, Sq]`` / ``[Hq, Tq]``."""
     p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
-                   max_seqlen_kv=max_seqlen_kv)
+                   max_seqlen_kv=max_seqlen_kv, cu_seqlens_q_padded=cu_seqlens_q_padded,
+                   cu_seqlens_kv_padded=cu_seqlens_kv_padded)
     thd = p.layout == _lib.ATTN_LAYOUT_THD
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
@@ -122,7 +133,8 @@ def attn_bwd_workspace_size(q, k, **kw) -> int:
 
 def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens_q=None,
              cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None, dk=None,
-             dv=None, workspace=None, deterministic=False, dlse=None
+             dv=None, workspace=None, deterministic=False, dlse=None,
+             cu_seqlens_q_padded=None, cu_seqlens_kv_padded=None
              ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Backward attention: ``(dq, dk, dv)`` for upstream gradient ``dout``
     (and ``dlse``, the gradient with respect to the forward's LSE output,
@@ -134,7 +146,9 @@ def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens
     runs."""
     p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
-                   max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
+                   max_seqlen_kv=max_seqlen_kv, deterministic=deterministic,
+                   cu_seqlens_q_padded=cu_seqlens_q_padded,
+                   cu_seqlens_kv_padded=cu_seqlens_kv_padded)
     thd = p.layout == _lib.ATTN_LAYOUT_THD
     lib = _lib.load()
     if dq is None:
@@ -163,7 +177,8 @@ def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens
 
 def attn_bwd_noalloc(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1),
                      cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None,
-                     max_seqlen_kv=None, dq=None, dk=None, dv=None, deterministic=False
+                     max_seqlen_kv=None, dq=None, dk=None, dv=None, deterministic=False,
+                     cu_seqlens_q_padded=None, cu_seqlens_kv_padded=None
                      ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """:func:`attn_bwd` for callers that cannot allocate device scratch: the
     library's own fixed scratch array (``_lib.NOALLOC_SCRATCH_BYTES`` bytes per
@@ -172,7 +187,9 @@ def attn_bwd_noalloc(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1),
     torch allocate dq/dk/dv when they are not passed.)"""
     p = params_for(q, k, scale=scale, window=window, cu_seqlens_q=cu_seqlens_q,
                    cu_seqlens_kv=cu_seqlens_kv, max_seqlen_q=max_seqlen_q,
-                   max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
+                   max_seqlen_kv=max_seqlen_kv, deterministic=deterministic,
+                   cu_seqlens_q_padded=cu_seqlens_q_padded,
+                   cu_seqlens_kv_padded=cu_seqlens_kv_padded)
     thd = p.layout == _lib.ATTN_LAYOUT_THD
     if dq is None:
         dq = torch.empty(q.shape, dtype=q.dtype, device=q.device)

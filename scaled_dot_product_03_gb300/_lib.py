@@ -40,7 +40,8 @@ class AttnParams(ctypes.Structure):
                 ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_kv", ctypes.c_void_p),
                 ("max_seqlen_q", ctypes.c_int), ("max_seqlen_kv", ctypes.c_int),
                 ("scale", ctypes.c_float), ("window_left", ctypes.c_int),
-                ("window_right", ctypes.c_int), ("deterministic", ctypes.c_int)]
+                ("window_right", ctypes.c_int), ("deterministic", ctypes.c_int),
+                ("cu_seqlens_q_padded", ctypes.c_void_p), ("cu_seqlens_kv_padded", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):

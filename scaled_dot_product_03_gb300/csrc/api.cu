@@ -90,6 +90,8 @@ attn_status check_params(const attn_params *p) {
             return fail(ATTN_ERR_INVALID_ARG, "negative max_seqlen");
         if (p->max_seqlen_q > p->Sq || p->max_seqlen_kv > p->Skv)
             return fail(ATTN_ERR_INVALID_ARG, "max_seqlen exceeds the total token rows");
+    } else if (p->cu_seqlens_q_padded || p->cu_seqlens_kv_padded) {
+        return fail(ATTN_ERR_INVALID_ARG, "padded cu_seqlens need the THD layout");
     }
     return ATTN_OK;
 }
@@ -148,6 +150,8 @@ Geometry geometry_of(const attn_params *p) {
     g.Tq = p->Sq;
     g.cu_q = p->cu_seqlens_q;
     g.cu_kv = p->cu_seqlens_kv;
+    g.pad_q = p->cu_seqlens_q_padded;
+    g.pad_kv = p->cu_seqlens_kv_padded;
     g.wl = p->window_left;
     g.wr = p->window_right;
     g.scale = p->scale;

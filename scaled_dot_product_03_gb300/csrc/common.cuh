@@ -31,6 +31,8 @@ struct Geometry {
     int thd;              // 1: packed THD, 0: dense
     int Tq;               // THD: total query rows (LSE row pitch)
     const int *cu_q, *cu_kv;
+    const int *pad_q, *pad_kv;  // THD: first row of each sequence when the
+                                // buffer is padded (null: cu_q / cu_kv)
     int wl, wr;           // window, -1 = unbounded
     float scale;
     float scale_log2;     // scale * log2(e)
@@ -44,10 +46,11 @@ struct SeqInfo {
 __device__ __forceinline__ SeqInfo seq_info(const Geometry &g, int b) {
     SeqInfo s;
     if (g.thd) {
-        s.q0 = __ldg(g.cu_q + b);
-        s.Lq = __ldg(g.cu_q + b + 1) - s.q0;
-        s.kv0 = __ldg(g.cu_kv + b);
-        s.Lkv = __ldg(g.cu_kv + b + 1) - s.kv0;
+        const int q_lo = __ldg(g.cu_q + b), kv_lo = __ldg(g.cu_kv + b);
+        s.Lq = __ldg(g.cu_q + b + 1) - q_lo;
+        s.Lkv = __ldg(g.cu_kv + b + 1) - kv_lo;
+        s.q0 = g.pad_q ? __ldg(g.pad_q + b) : q_lo;
+        s.kv0 = g.pad_kv ? __ldg(g.pad_kv + b) : kv_lo;
     } else {
         s.q0 = 0;
         s.kv0 = 0;

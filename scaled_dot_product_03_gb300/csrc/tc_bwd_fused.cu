@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float
     constexpr int C = D / 8;
     const int64_t rows = g.thd ? (int64_t)g.Hq * g.Tq : (int64_t)g.B * g.Hq * g.Sq;
     const int64_t n = rows * C;
-    const int t_end = g.thd ? __ldg(g.cu_q + g.B) : 0;
+
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = idx / C;
@@ -545,7 +545,17 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float
             h = (int)(r / g.Tq);
             srow = (int)(r % g.Tq);
             b = 0;
-            if (srow >= t_end) continue;  // token rows outside every sequence are not written
+            // token rows outside every sequence (the tail, or the gaps of a
+            // padded buffer) are not written: find the last sequence that
+            // starts at or before the row
+            const int *start = g.pad_q ? g.pad_q : g.cu_q;
+            int lo = 0, hi = g.B - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) / 2;
+                if (__ldg(start + mid) <= srow) lo = mid; else hi = mid - 1;
+            }
+            const int len = __ldg(g.cu_q + lo + 1) - __ldg(g.cu_q + lo);
+            if (g.B <= 0 || srow < __ldg(start + lo) || srow >= __ldg(start + lo) + len) continue;
         } else {
             const int64_t bhr = r / g.Sq;
             srow = (int)(r % g.Sq);

@@ -73,6 +73,7 @@ def _t(ptr=4096, strides=(32768, 256, 64, 1)):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(deterministic=2), _lib.ATTN_ERR_INVALID_ARG),
+    (dict(cu_seqlens_q_padded=4096), _lib.ATTN_ERR_INVALID_ARG),   # padding needs THD
     (dict(D=96), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(D=0), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(Hq=3, Hkv=2), _lib.ATTN_ERR_INVALID_ARG),

@@ -307,3 +307,68 @@ def test_watchdog_gives_up_and_reports():
     o, lse = run_fwd(_dev(prob))
     _sync_ok()
     check_fwd(prob, o, lse)
+
+
+# ------------------------------------------------------- padded cu_seqlens
+
+@pytest.mark.parametrize("dtype,D,det", [(torch.bfloat16, 128, False), (torch.bfloat16, 128, True),
+                                         (torch.float16, 64, False), (torch.float32, 64, False)])
+def test_thd_padded_cu_seqlens(dtype, D, det):
+    """THD buffers with padding between sequences (cu_seqlens_*_padded of the
+    THD+CP thread): sequence b occupies rows [pad[b], pad[b] + L_b).  Outputs
+    on the sequence rows equal the unpadded problem's oracle; rows in the
+    gaps (finite filler) are never written."""
+    lengths = [300, 1, 517, 64, 0, 129]
+    prob = inputs.varlen(lengths=lengths, Hq=4, Hkv=2, D=D, dtype=dtype, seed=41, dout_seed=42)
+    cu_h = [0]
+    for L in lengths:
+        cu_h.append(cu_h[-1] + L)
+    pads = [0]
+    for L in lengths:  # each sequence rounded up to 64 rows, plus 7
+        pads.append(pads[-1] + (L + 63) // 64 * 64 + 7)
+    Tp = pads[-1]
+
+    def scatter(t, fill):
+        out = torch.full((Tp,) + tuple(t.shape[1:]), fill, dtype=t.dtype)
+        for b, L in enumerate(lengths):
+            out[pads[b]:pads[b] + L] = t[cu_h[b]:cu_h[b] + L]
+        return out.to(DEV)
+
+    def gather(t):
+        return torch.cat([t[pads[b]:pads[b] + L] for b, L in enumerate(lengths)])
+
+    q, k, v, dout = (scatter(getattr(prob, n), 0.5) for n in ("q", "k", "v", "dout"))
+    cu_d = torch.tensor(cu_h, dtype=torch.int32, device=DEV)
+    pad_d = torch.tensor(pads, dtype=torch.int32, device=DEV)
+    sentinel = 7.0
+    o = torch.full_like(q, sentinel)
+    lse = torch.full((prob.Hq, Tp), sentinel, dtype=torch.float32, device=DEV)
+    dq, dk, dv = (torch.full_like(t, sentinel) for t in (q, k, v))
+    args = dict(scale=prob.scale, window=prob.window, cu_seqlens_q=cu_d, cu_seqlens_kv=cu_d,
+                max_seqlen_q=max(lengths), max_seqlen_kv=max(lengths),
+                cu_seqlens_q_padded=pad_d, cu_seqlens_kv_padded=pad_d)
+    gb.attn_fwd(q, k, v, out=o, lse=lse, **args)
+    gb.attn_bwd(dout, q, k, v, o, lse, dq=dq, dk=dk, dv=dv, deterministic=det, **args)
+    _sync_ok()
+    rows = torch.cat([torch.arange(pads[b], pads[b] + L) for b, L in enumerate(lengths)])
+    check_fwd(prob, gather(o), lse[:, rows.to(DEV)])
+    check_bwd(prob, gather(dq), gather(dk), gather(dv))
+    gap = torch.ones(Tp, dtype=torch.bool)
+    gap[rows] = False
+    gap = gap.to(DEV)
+    for t in (o, dq, dk, dv):
+        assert torch.all(t[gap] == sentinel)
+    assert torch.all(lse[:, gap] == sentinel)
+
+
+def test_cross_attention_few_queries_many_keys():
+    """Cross attention of a few decoder positions over a long encoder
+    sequence (the RETURNN pull request's seqlen_kv, beam-search shapes):
+    Sq = 7, Skv = 1024, no mask, grouped heads."""
+    prob = inputs.dense(3, 7, 8, 128, Hkv=2, Skv=1024, window=(-1, -1), seed=51, dout_seed=52)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
