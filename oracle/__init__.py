@@ -175,3 +175,65 @@ def merge_lse_bwd(o1, lse1, o2, lse2, dout, dlse=None):
                                  _ptr(dout), _ptr(dlse), _ptr(do1), _ptr(dl1),
                                  _ptr(do2), _ptr(dl2))
     return do1, dl1, do2, dl2
+
+
+# ---------------------------------------------------------------------------
+# Context parallelism over THD ("[PyTorch] Add support for cuDNN
+# FusedAttention + THD + CP": every sequence is split into CP*2 chunks and
+# each rank is given 2 of them for load balance; K/V move around a ring of
+# ranks and each rank merges its partial results; the order of the ring
+# does not matter).  Plain loops, float64, on gathered copies of the chunks.
+
+def thd_partitioned_indices(cu_seqlens_padded, total_tokens, world_size, rank):
+    """Rows of the padded THD buffer held by ``rank``: for every sequence,
+    the rows of chunk ``rank`` then of chunk ``2 * world_size - 1 - rank``
+    of its 2 * world_size equal chunks."""
+    pads = [int(x) for x in cu_seqlens_padded]
+    assert pads[-1] == total_tokens
+    n = 2 * world_size
+    rows = []
+    for b in range(len(pads) - 1):
+        size = (pads[b + 1] - pads[b]) // n
+        for c in (rank, n - 1 - rank):
+            rows.extend(range(pads[b] + c * size, pads[b] + (c + 1) * size))
+    return np.array(rows, dtype=np.int64)
+
+
+def ring_attention_fwd(q, k, v, cu_seqlens, cu_seqlens_padded, cp_size, scale, causal=True):
+    """Every rank's ring, as float64 partial attentions merged by LSE.
+    q, k, v: padded THD ``[T, H, D]``; returns ``(o [T, Hq, D], lse [T, Hq])``
+    with o = 0, lse = -inf on padding rows.  A query chunk at sequence
+    offset a against a key chunk at offset c sees key j from query i iff
+    a + i >= c + j (causal), i.e. window (-1, a - c); pairs with a < c see
+    nothing."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lens = np.diff(np.asarray(cu_seqlens, dtype=np.int64))
+    pads = [int(x) for x in cu_seqlens_padded]
+    T, Hq, D = q.shape
+    n = 2 * cp_size
+    o = np.zeros((T, Hq, D))
+    lse = np.full((T, Hq), -np.inf)
+    for rank in range(cp_size):
+        for b, L in enumerate(lens):
+            size = (pads[b + 1] - pads[b]) // n
+            for cq in (rank, n - 1 - rank):
+                a = cq * size
+                nq = max(0, min(size, L - a))
+                if nq == 0:
+                    continue
+                rows = np.arange(pads[b] + a, pads[b] + a + nq)
+                acc_o, acc_l = np.zeros((nq, Hq, D)), np.full((nq, Hq), -np.inf)
+                for step in range(cp_size):           # K/V of rank (rank - step) mod CP
+                    src = (rank - step) % cp_size
+                    for ck in (src, n - 1 - src):
+                        c = ck * size
+                        nk = max(0, min(size, L - c))
+                        if nk == 0 or (causal and a < c):
+                            continue
+                        kr = np.arange(pads[b] + c, pads[b] + c + nk)
+                        window = (-1, a - c) if causal else (-1, -1)
+                        po, pl = attn_fwd(q[rows], k[kr], v[kr], np.array([0, nq]),
+                                          np.array([0, nk]), scale, window)
+                        acc_o, acc_l = merge_lse(acc_o, acc_l, po, pl)
+                o[rows], lse[rows] = acc_o, acc_l
+    return o, lse

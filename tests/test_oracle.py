@@ -459,3 +459,56 @@ def test_page1_views_have_the_printed_strides():
         sbhd = (t.stride(1), t.stride(0), t.stride(2), t.stride(3))
         assert sbhd == strides, (n, sbhd)
     assert prob.k.storage_offset() == 16 * 64 and prob.v.storage_offset() == 17 * 64
+
+
+# -- 11. context parallelism over THD (the THD+CP thread) --------------------
+
+def _padded(lengths, multiple):
+    pads = [0]
+    for L in lengths:
+        pads.append(pads[-1] + -(-max(L, 1) // multiple) * multiple)
+    return pads
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 4])
+def test_partitioned_indices_cover_and_balance(world):
+    """Every row of the padded buffer belongs to exactly one rank, every rank
+    holds the same number of rows, two chunks per sequence, and (the point
+    of the split) the same causal work: the sum over its rows of the number
+    of keys a row sees under a causal mask."""
+    lengths = [8 * world, 24 * world, 2 * world]
+    pads = _padded(lengths, 2 * world)
+    T = pads[-1]
+    parts = [oracle.thd_partitioned_indices(pads, T, world, r) for r in range(world)]
+    allrows = np.sort(np.concatenate(parts))
+    np.testing.assert_array_equal(allrows, np.arange(T))
+    assert len({len(p) for p in parts}) == 1
+    work = []
+    for p in parts:
+        w = 0
+        for row in p:
+            b = int(np.searchsorted(pads, row, side="right") - 1)
+            w += row - pads[b] + 1           # keys seen by this row (causal)
+        work.append(w)
+    assert len(set(work)) == 1, work
+
+
+@pytest.mark.parametrize("cp", [2, 3])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_attention_equals_full_attention(cp, causal):
+    """The ring of partial attentions merged by LSE equals one attention over
+    each whole sequence; padding rows stay (0, -inf)."""
+    lengths = [37, 1, 64, 0, 50]
+    pads = _padded(lengths, 2 * cp)
+    T, H, Hkv, D, scale = pads[-1], 4, 2, 8, 0.45
+    g = np.random.default_rng(5)
+    q, k, v = g.standard_normal((T, H, D)), g.standard_normal((T, Hkv, D)), g.standard_normal((T, Hkv, D))
+    cu_l = np.concatenate([[0], np.cumsum(lengths)])
+    o, lse = oracle.ring_attention_fwd(q, k, v, cu_l, pads, cp, scale, causal)
+    rows = np.concatenate([np.arange(pads[b], pads[b] + L) for b, L in enumerate(lengths)])
+    o_full, lse_full = oracle.attn_fwd(q[rows], k[rows], v[rows], cu_l, cu_l, scale,
+                                       (-1, 0) if causal else (-1, -1))
+    np.testing.assert_allclose(o[rows], o_full, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse[rows], lse_full, rtol=1e-12, atol=1e-13)
+    pad_rows = np.setdiff1d(np.arange(T), rows)
+    assert np.all(o[pad_rows] == 0) and np.all(np.isneginf(lse[pad_rows]))
