@@ -232,6 +232,22 @@ GBATTN_API attn_status attn_merge_lse_bwd(attn_dtype dtype, int B, int S, int H,
                                float *dlse2, attn_stream_t stream);
 
 /*
+ * Token rows of a padded THD buffer that rank `rank` of `world_size` holds
+ * under the load-balanced context-parallel split of "[PyTorch] Add support
+ * for cuDNN FusedAttention + THD + CP" (its thd_get_partitioned_indices):
+ * every sequence b, padded to cu_seqlens_padded[b+1] - cu_seqlens_padded[b]
+ * rows (a multiple of 2 x world_size), is cut into 2 x world_size equal
+ * chunks and the rank holds chunk `rank` and chunk 2 x world_size - 1 -
+ * rank.  indices (device, int32, total_tokens / world_size entries)
+ * receives, sequence by sequence, the rows of the first chunk then of the
+ * second.  cu_seqlens_padded: device, B + 1 entries from 0 to total_tokens;
+ * the per-sequence multiples are the caller's to ensure.
+ */
+GBATTN_API attn_status attn_thd_partitioned_indices(const int32_t *cu_seqlens_padded, int B,
+                                         int total_tokens, int world_size, int rank,
+                                         int32_t *indices, attn_stream_t stream);
+
+/*
  * Per-launch timing, for benchmarks and profilers.  After
  * attn_profile_begin(n) the calling thread's next (at most n) kernel
  * launches by this library are each bracketed by two CUDA events recorded

@@ -22,7 +22,8 @@ ATTN_LAYOUT_DENSE4D, ATTN_LAYOUT_THD = 0, 1
 EXPORTS = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_merge_lse",
            "attn_last_error_string", "attn_check_device_error", "attn_set_watchdog_ns",
            "attn_watchdog_selftest", "attn_profile_begin", "attn_profile_read",
-           "attn_bwd_noalloc", "attn_bwd_dlse", "attn_merge_lse_bwd")
+           "attn_bwd_noalloc", "attn_bwd_dlse", "attn_merge_lse_bwd",
+           "attn_thd_partitioned_indices")
 KERNEL_KINDS = {0: "fwd", 1: "bwd_preprocess", 2: "bwd_dkdv", 3: "bwd_dq", 4: "merge",
                 5: "simt_fwd", 6: "simt_bwd_dq", 7: "simt_bwd_dkdv", 8: "bwd_fused",
                 9: "bwd_dq_convert", 10: "merge_bwd"}
@@ -82,6 +83,9 @@ def load(path: str = LIB_PATH):
         lib.attn_merge_lse_bwd.argtypes = [i32, i32, i32, i32, i32, T, f32p, T, f32p, T, f32p,
                                            T, f32p, T, f32p, S]
         lib.attn_merge_lse_bwd.restype = i32
+        lib.attn_thd_partitioned_indices.argtypes = [ctypes.c_void_p, i32, i32, i32, i32,
+                                                     ctypes.c_void_p, S]
+        lib.attn_thd_partitioned_indices.restype = i32
         lib.attn_last_error_string.argtypes = []
         lib.attn_last_error_string.restype = ctypes.c_char_p
         lib.attn_check_device_error.argtypes = [S]

@@ -435,6 +435,25 @@ attn_status attn_merge_lse_bwd(attn_dtype dtype, int B, int S, int H, int D, att
     return ATTN_OK;
 }
 
+attn_status attn_thd_partitioned_indices(const int32_t *cu_seqlens_padded, int B, int total_tokens,
+                                         int world_size, int rank, int32_t *indices,
+                                         attn_stream_t stream) {
+    t_error.clear();
+    if (world_size < 1 || rank < 0 || rank >= world_size)
+        return fail(ATTN_ERR_INVALID_ARG, "rank %d of world size %d", rank, world_size);
+    if (B < 0 || total_tokens < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size");
+    if (total_tokens % (2 * world_size))
+        return fail(ATTN_ERR_INVALID_ARG, "total_tokens %d is not a multiple of 2 x world size %d",
+                    total_tokens, world_size);
+    if (total_tokens == 0) return ATTN_OK;
+    if (B < 1 || !cu_seqlens_padded || !indices)
+        return fail(ATTN_ERR_INVALID_ARG, "need B >= 1 and non-NULL cu_seqlens_padded, indices");
+    cudaError_t e = launch_partitioned_indices(cu_seqlens_padded, B, world_size, rank,
+                                               total_tokens / world_size, indices, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_thd_partitioned_indices launch");
+    return ATTN_OK;
+}
+
 attn_status attn_profile_begin(int max_launches) {
     t_error.clear();
     if (max_launches < 1) return fail(ATTN_ERR_INVALID_ARG, "max_launches must be positive");

@@ -51,5 +51,7 @@ struct MergeBwdArgs {
     float *dlse1, *dlse2;
 };
 cudaError_t launch_merge_bwd(int dtype, const MergeBwdArgs &a, cudaStream_t st);
+cudaError_t launch_partitioned_indices(const int *pad, int B, int world, int rank, int n_out, int *out,
+                                       cudaStream_t st);
 
 }  // namespace gbattn

@@ -165,3 +165,12 @@ def test_merge_rejects_bad_args(lib):
     assert lib.attn_merge_lse(1, 1, 1, 1, 300, t, 4096, t, 4096, t, 4096, None) == \
         _lib.ATTN_ERR_UNSUPPORTED
     assert lib.attn_merge_lse(1, 0, 5, 1, 64, t, 4096, t, 4096, t, 4096, None) == _lib.ATTN_OK
+
+
+def test_partitioned_indices_rejects_bad_args(lib):
+    f = lib.attn_thd_partitioned_indices
+    assert f(4096, 1, 16, 0, 0, 4096, None) == _lib.ATTN_ERR_INVALID_ARG   # world 0
+    assert f(4096, 1, 16, 2, 2, 4096, None) == _lib.ATTN_ERR_INVALID_ARG   # rank >= world
+    assert f(4096, 1, 18, 4, 0, 4096, None) == _lib.ATTN_ERR_INVALID_ARG   # 18 % 8 != 0
+    assert f(None, 1, 16, 2, 0, 4096, None) == _lib.ATTN_ERR_INVALID_ARG   # NULL offsets
+    assert f(None, 0, 0, 2, 1, None, None) == _lib.ATTN_OK                 # empty: nothing
