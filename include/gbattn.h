@@ -114,7 +114,8 @@ typedef struct {
     int Sq, Skv;         /* DENSE4D: sequence lengths.  THD: total token rows
                             Tq and Tkv of the packed q and k/v tensors */
     int Hq, Hkv;         /* query heads, key/value heads (Hq % Hkv == 0) */
-    int D;               /* head dimension: 64 or 128 */
+    int D;               /* head dimension: 32, 64, 96 or 128 (tensor cores for
+                            fp16 / bf16 at 64 and 128; FFMA kernels otherwise) */
     const int32_t *cu_seqlens_q;  /* THD only: device, B + 1 non-decreasing */
     const int32_t *cu_seqlens_kv; /* offsets starting at 0 (NULL for DENSE4D) */
     int max_seqlen_q;    /* THD only: upper bound of the sequence lengths */

@@ -74,8 +74,8 @@ attn_status check_params(const attn_params *p) {
         return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d Sq=%d Skv=%d)", p->B, p->Sq, p->Skv);
     if (p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0)
         return fail(ATTN_ERR_INVALID_ARG, "Hq=%d must be a positive multiple of Hkv=%d", p->Hq, p->Hkv);
-    if (p->D != 64 && p->D != 128)
-        return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", p->D);
+    if (p->D != 32 && p->D != 64 && p->D != 96 && p->D != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (32, 64, 96 or 128)", p->D);
     if (p->deterministic != 0 && p->deterministic != 1)
         return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
     if (p->window_left < -1 || p->window_right < -1)

@@ -111,6 +111,15 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Lanes that share one row: the largest power of two (the group is reduced
+// with xor shuffles and must tile the warp) not above the row's chunks,
+// at most 32; lanes loop over the remaining chunks.
+__host__ __device__ inline int lanes_per_row(int chunks) {
+    int t = 1;
+    while (t * 2 <= chunks && t < 32) t *= 2;
+    return t;
+}
+
 // Backward preprocess: delta = <dO, O> - dLSE per (row, head) (dLSE = 0 when
 // no LSE gradient is given).  A group of up to 32
 // lanes (power of two) covers one (row, head), each lane VEC elements at a
@@ -122,7 +131,7 @@ __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
     const Geometry &g = a.g;
     const int D = g.D;
     const int chunks = D / VEC;
-    const int tpr = chunks < 32 ? chunks : 32;
+    const int tpr = lanes_per_row(chunks);
     const int lane = threadIdx.x & 31, sub = lane / tpr, c0 = lane % tpr;
     const int per_warp = 32 / tpr;
     const int64_t pairs = (int64_t)rows * g.Hq;
@@ -378,15 +387,24 @@ cudaError_t bwd_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st
 
 }  // namespace
 
+// Head dims with a kernel: 64 and 128 (also served by the tensor-core
+// kernels for 16-bit types) and 32, 96 (this path only, for every type).
+template <int D>
+cudaError_t fwd_dtype(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st) {
+    switch (dtype) {
+        case 0: return fwd_typed<__half, D>(a, max_lq, st);
+        case 1: return fwd_typed<__nv_bfloat16, D>(a, max_lq, st);
+        case 2: return fwd_typed<float, D>(a, max_lq, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_simt_fwd(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st) {
-    const int D = a.g.D;
-    switch (dtype * 2 + (D == 128)) {
-        case 0: return fwd_typed<__half, 64>(a, max_lq, st);
-        case 1: return fwd_typed<__half, 128>(a, max_lq, st);
-        case 2: return fwd_typed<__nv_bfloat16, 64>(a, max_lq, st);
-        case 3: return fwd_typed<__nv_bfloat16, 128>(a, max_lq, st);
-        case 4: return fwd_typed<float, 64>(a, max_lq, st);
-        case 5: return fwd_typed<float, 128>(a, max_lq, st);
+    switch (a.g.D) {
+        case 32: return fwd_dtype<32>(dtype, a, max_lq, st);
+        case 64: return fwd_dtype<64>(dtype, a, max_lq, st);
+        case 96: return fwd_dtype<96>(dtype, a, max_lq, st);
+        case 128: return fwd_dtype<128>(dtype, a, max_lq, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -398,7 +416,7 @@ bool rows_aligned16(const View &v, size_t es) {
 }
 template <typename T, int VEC>
 void preprocess_typed(const BwdArgs &a, int rows, cudaStream_t st) {
-    const int tpr = (a.g.D / VEC) < 32 ? a.g.D / VEC : 32;
+    const int tpr = lanes_per_row(a.g.D / VEC);
     const int64_t warps = ((int64_t)rows * a.g.Hq + (32 / tpr) - 1) / (32 / tpr);
     int64_t blocks = (warps + 7) / 8;
     if (blocks > 152 * 16) blocks = 152 * 16;
@@ -424,16 +442,23 @@ cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStr
     return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t bwd_dtype(int dtype, const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
+    switch (dtype) {
+        case 0: return bwd_typed<__half, D>(a, max_lq, max_lkv, st);
+        case 1: return bwd_typed<__nv_bfloat16, D>(a, max_lq, max_lkv, st);
+        case 2: return bwd_typed<float, D>(a, max_lq, max_lkv, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv,
                             cudaStream_t st) {
-    const int D = a.g.D;
-    switch (dtype * 2 + (D == 128)) {
-        case 0: return bwd_typed<__half, 64>(a, max_lq, max_lkv, st);
-        case 1: return bwd_typed<__half, 128>(a, max_lq, max_lkv, st);
-        case 2: return bwd_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, st);
-        case 3: return bwd_typed<__nv_bfloat16, 128>(a, max_lq, max_lkv, st);
-        case 4: return bwd_typed<float, 64>(a, max_lq, max_lkv, st);
-        case 5: return bwd_typed<float, 128>(a, max_lq, max_lkv, st);
+    switch (a.g.D) {
+        case 32: return bwd_dtype<32>(dtype, a, max_lq, max_lkv, st);
+        case 64: return bwd_dtype<64>(dtype, a, max_lq, max_lkv, st);
+        case 96: return bwd_dtype<96>(dtype, a, max_lq, max_lkv, st);
+        case 128: return bwd_dtype<128>(dtype, a, max_lq, max_lkv, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -74,7 +74,7 @@ def _t(ptr=4096, strides=(32768, 256, 64, 1)):
 @pytest.mark.parametrize("kw,status", [
     (dict(deterministic=2), _lib.ATTN_ERR_INVALID_ARG),
     (dict(cu_seqlens_q_padded=4096), _lib.ATTN_ERR_INVALID_ARG),   # padding needs THD
-    (dict(D=96), _lib.ATTN_ERR_UNSUPPORTED),
+    (dict(D=80), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(D=0), _lib.ATTN_ERR_UNSUPPORTED),
     (dict(Hq=3, Hkv=2), _lib.ATTN_ERR_INVALID_ARG),
     (dict(Hkv=0), _lib.ATTN_ERR_INVALID_ARG),
@@ -139,7 +139,7 @@ def test_lse_gradient_backward_rejects_like_attn_bwd(lib):
     """attn_bwd_dlse validates exactly as attn_bwd (nothing is launched)."""
     t = _t()
     for kw, status in ((dict(deterministic=2), _lib.ATTN_ERR_INVALID_ARG),
-                       (dict(D=96), _lib.ATTN_ERR_UNSUPPORTED)):
+                       (dict(D=80), _lib.ATTN_ERR_UNSUPPORTED)):
         p = _params(**kw)
         st = lib.attn_bwd_dlse(ctypes.byref(p), t, t, t, t, t, 4096, 4096, t, t, t, 4096, 1 << 20,
                                None)

@@ -372,3 +372,25 @@ def test_cross_attention_few_queries_many_keys():
     _sync_ok()
     check_fwd(prob, o, lse)
     check_bwd(prob, dq, dk, dv)
+
+
+# -------------------------------------------------------- other head dims
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("D", [32, 96])
+@pytest.mark.parametrize("case", [
+    dict(B=2, Sq=150, Skv=150, Hq=4, Hkv=2, window=(-1, 0)),
+    dict(B=1, Sq=70, Skv=201, Hq=2, Hkv=1, window=(-1, -1)),
+    dict(B=1, Sq=260, Skv=260, Hq=2, Hkv=2, window=(17, 3)),
+])
+def test_head_dims_32_and_96(dtype, D, case):
+    """Head dims outside the tensor-core kernels run on the FFMA kernels for
+    every element type (forward, backward, merge)."""
+    prob = inputs.dense(case["B"], case["Sq"], case["Hq"], D, dtype=dtype, window=case["window"],
+                        Hkv=case["Hkv"], Skv=case["Skv"], seed=D + case["Sq"])
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
