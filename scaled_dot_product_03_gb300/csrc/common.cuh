@@ -92,14 +92,17 @@ __device__ __forceinline__ void query_range(int j0, int j1, int Lq, int wl, int 
 // pairs: the work in flight at one time then touches a few heads' tensors
 // (they stay in L2), and inside a band the tiles go by rank 0 (heaviest)
 // first, each rank across the band's heads, so dispatch stays close to
-// longest-first.
+// longest-first.  Measured: 8 suits the forward and the two-kernel
+// backward; the single-pass backward, whose fp32 dQ sums also live in L2,
+// prefers fewer heads per band.
 constexpr int kHeadBand = 8;
 
-__device__ __forceinline__ void banded_order(int w, int nt, int nbh, int &bh, int &rank) {
-    const int per_band = kHeadBand * nt;
+__device__ __forceinline__ void banded_order(int w, int nt, int nbh, int &bh, int &rank,
+                                             int band = kHeadBand) {
+    const int per_band = band * nt;
     const int bi = w / per_band, r = w % per_band;
-    const int h0 = bi * kHeadBand;
-    const int bs = min(kHeadBand, nbh - h0);
+    const int h0 = bi * band;
+    const int bs = min(band, nbh - h0);
     rank = r / bs;
     bh = h0 + r % bs;
 }

@@ -54,6 +54,7 @@ constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDrainWarp0 = 10;
 constexpr int kDrain = 128;
+constexpr int kFusedHeadBand = 4;  // heads per band of the work order (see banded_order)
 
 constexpr int kKVTile = BK * D * 2;   // 32 KB
 constexpr int kQTile = BQ * D * 2;    // 16 KB
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // banded work order; rank 0 = the first key tiles (seen by the most
     // queries when causal)
     int bh, kt;
-    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B, bh, kt);
+    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B, bh, kt, kFusedHeadBand);
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BK;
