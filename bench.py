@@ -113,15 +113,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(args):
+def dist_setup(args, backend="nccl"):
+    """Rank, world size and local rank from the torchrun environment; one
+    process group per job (NCCL across GPUs; gloo for the CPU tests)."""
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
     return ws, rank, local
 
 
@@ -132,13 +135,22 @@ def barrier(ws):
 
 
 def max_over_ranks(x, ws):
+    """The slowest rank's time: the job is done when every rank is."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(ws, flops_per_rank_step, ms_per_step):
+    """Whole-job TFLOP/s: every rank processes its own (weak-scaled) batch of
+    flops_per_rank_step in each step, and a step takes ms_per_step (the max
+    over ranks)."""
+    return ws * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
 def run_ours(args):
@@ -212,7 +224,7 @@ def run_ours(args):
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     f_fwd, f_bwd, nvis = flops(B, S, H, D, win)
     ms_step = ms_total / args.steps
-    tflops = ws * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    tflops = job_throughput(ws, f_fwd + f_bwd, ms_step)
     peaks, src = measured_peaks()
     peak_bf16 = peaks.get("bf16_tflops_sustained" if args.steps * ms_step > 2000 else "bf16_tflops")
     # per-kernel launch statistics; flops each kernel executes and the part of
@@ -297,7 +309,7 @@ def run_ours(args):
         e2e_ms = max_over_ranks(s2.elapsed_time(e2), ws) / args.steps
         # the results are those of the device-resident step
         assert torch.equal(sets[0]["o"], sets[1]["o"]) or args.steps < 2
-    e2e_tflops = ws * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12 if e2e_ms == e2e_ms else None
+    e2e_tflops = job_throughput(ws, f_fwd + f_bwd, e2e_ms) if e2e_ms == e2e_ms else None
 
     aux = aux_lines(gb, inputs, dev, peaks) if rank == 0 and not args.no_aux else {}
     if rank == 0 and not args.no_aux:
