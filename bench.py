@@ -247,6 +247,17 @@ def run_ours(args):
         if name in exec_flops:
             kernels[name]["executed_tflops"] = round(exec_flops[name] / (m * 1e-3) / 1e12, 1)
             kernels[name]["algorithmic_tflops"] = round(alg_flops[name] / (m * 1e-3) / 1e12, 1)
+    # HBM-bound kernels: algorithmic bytes per launch and achieved GB/s
+    # (preprocess: reads O and dO, writes delta and clears the fp32 dq
+    # accumulator; convert: reads the accumulator, writes dq)
+    elt, rows = 2, B * H * S
+    hbm_bytes = {"bwd_preprocess": rows * (2 * D * elt + 4 + 4 * D),
+                 "bwd_dq_convert": rows * (4 * D + D * elt)}
+    for name, nbytes in hbm_bytes.items():
+        if name in kernels:
+            gbs = nbytes / (kernels[name]["mean_ms"] * 1e-3) / 1e9
+            kernels[name].update({"algorithmic_bytes": nbytes, "GB/s": round(gbs, 1),
+                                  "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)})
     dominant = max(kern, key=lambda k: sum(kern[k]))
 
     # ------------------------------------------------------------- end to end
