@@ -144,8 +144,8 @@ GBATTN_API attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor
  * Bytes of device scratch memory attn_bwd needs for these parameters: the
  * fp32 row terms delta_i = <dO_i, O_i> (one per query row and head) and,
  * when the single-pass backward applies (deterministic == 0, fp16 / bf16,
- * D = 128, at least one query row), an fp32 dq accumulator of D floats per
- * query row and head.  Returns 0 for invalid parameters.
+ * D = 64 or 128, at least one query row), an fp32 dq accumulator of D
+ * floats per query row and head.  Returns 0 for invalid parameters.
  */
 GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
 
@@ -160,11 +160,11 @@ GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
  * shape, dk and dv k's shape, each with its own strides (they may be views
  * of one packed gradient buffer).
  * Determinism.  With p->deterministic = 0 and fp16 / bf16 inputs of head
- * dim 128, one pass over the (key block, query block) pairs forms S and dP
+ * dim 64 or 128, one pass over the (key block, query block) pairs forms S and dP
  * once and adds each pair's share of dq into an fp32 accumulator in the
  * workspace; those fp32 additions happen in an order set by the GPU's
  * scheduling, so dq may differ between runs in its last bits (dk and dv do
- * not).  In every other case (p->deterministic = 1, fp32, D = 64) every
+ * not).  In every other case (p->deterministic = 1, fp32, D = 32 or 96) every
  * output element is written by exactly one thread of one kernel and the
  * results do not depend on scheduling.  workspace: device memory of at least
  * attn_bwd_workspace_size(p) bytes, 256-byte aligned, whose contents on

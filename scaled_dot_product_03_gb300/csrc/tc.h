@@ -17,6 +17,10 @@ cudaError_t launch_tc_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, 
 // Single-pass backward: needs a.dq_acc (fp32, laid out like LSE with D
 // columns per row) cleared beforehand; writes dk, dv and then dq.
 cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, cudaStream_t st);
+// The head-dim-64 form of the single-pass backward (one launch, no convert).
+cudaError_t launch_tc_bwd_fused64(int dtype, const BwdArgs &a, int max_lkv, cudaStream_t st);
+// dq = scale * accumulator, in dq's element type and strides (D = 64 or 128).
+cudaError_t launch_dq_convert(int dtype, const BwdArgs &a, cudaStream_t st);
 
 // One kernel that waits on an mbarrier nothing arrives on, gives up after
 // `limit_ns`, and records the timeout in *err.

@@ -531,9 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // dq = scale * acc in the element type, acc laid out like LSE with D columns
 // per row.  8 head dims per thread (two 16-byte loads, one 16-byte store).
-template <typename T>
+template <typename T, int DD>
 __global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float *__restrict__ acc, Geometry g) {
-    constexpr int C = D / 8;
+    constexpr int C = DD / 8;
     const int64_t rows = g.thd ? (int64_t)g.Hq * g.Tq : (int64_t)g.B * g.Hq * g.Sq;
     const int64_t n = rows * C;
 
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float
             b = (int)(bhr / g.Hq);
             h = (int)(bhr % g.Hq);
         }
-        const float4 *src = reinterpret_cast<const float4 *>(acc + r * D + c * 8);
+        const float4 *src = reinterpret_cast<const float4 *>(acc + r * DD + c * 8);
         const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
         uint4 y;
         y.x = pack2<T>(x0.x * g.scale, x0.y * g.scale);
@@ -619,25 +619,42 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const int64_t n = (int64_t)acc_rows * acc_heads * (D / 8);
+    return launch_dq_convert(dt, a, st);
+}
+
+template <typename T, int DD>
+cudaError_t dq_convert_typed(const BwdArgs &a, cudaStream_t st) {
+    const Geometry &g = a.g;
+    const int64_t rows = g.thd ? (int64_t)g.Hq * g.Tq : (int64_t)g.B * g.Hq * g.Sq;
+    const int64_t n = rows * (DD / 8);
     int64_t blocks = (n + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
-    if (blocks > 0) {
-        prof_before(st, kProfBwdDqConvert);
-        dq_convert_kernel<T><<<(unsigned)blocks, 256, 0, st>>>(a.dq, a.dq_acc, g);
-        prof_after(st);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    if (blocks <= 0) return cudaSuccess;
+    prof_before(st, kProfBwdDqConvert);
+    dq_convert_kernel<T, DD><<<(unsigned)blocks, 256, 0, st>>>(a.dq, a.dq_acc, g);
+    prof_after(st);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-bool uses_tc_bwd_fused(int dtype, int D_) { return (dtype == 0 || dtype == 1) && D_ == D; }
+cudaError_t launch_dq_convert(int dtype, const BwdArgs &a, cudaStream_t st) {
+    switch (dtype * 2 + (a.g.D == 128)) {
+        case 0: return dq_convert_typed<__half, 64>(a, st);
+        case 1: return dq_convert_typed<__half, 128>(a, st);
+        case 2: return dq_convert_typed<__nv_bfloat16, 64>(a, st);
+        case 3: return dq_convert_typed<__nv_bfloat16, 128>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool uses_tc_bwd_fused(int dtype, int D_) { return (dtype == 0 || dtype == 1) && (D_ == 128 || D_ == 64); }
 
 cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, cudaStream_t st) {
     // callers route problems without query rows to the two-kernel backward
-    if (a.g.D != D || !a.dq_acc || (a.g.thd ? a.g.Tq : a.g.Sq) <= 0) return cudaErrorInvalidValue;
+    if (!a.dq_acc || (a.g.thd ? a.g.Tq : a.g.Sq) <= 0) return cudaErrorInvalidValue;
+    if (a.g.D == 64) return launch_tc_bwd_fused64(dtype, a, max_lkv, st);
+    if (a.g.D != D) return cudaErrorInvalidValue;
     switch (dtype) {
         case 0: return launch_typed<__half>(a, max_lkv, st);
         case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, st);

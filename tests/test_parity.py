@@ -124,9 +124,10 @@ def test_varlen_thd_gqa_fwd_bwd_sampled(det):
 
 # ---------------------------------------------------------------- edge cases
 
-# (dtype, D, deterministic): the 16-bit D=128 backward has a single-pass
-# and a two-kernel (bitwise reproducible) form; the others have one form.
+# (dtype, D, deterministic): the 16-bit backward at D=64 and 128 has a
+# single-pass and a two-kernel (bitwise reproducible) form; fp32 has one.
 _EDGE_KINDS = [(torch.float16, 64, False), (torch.bfloat16, 64, False), (torch.float32, 64, False),
+               (torch.bfloat16, 64, True),
                (torch.float16, 128, False), (torch.bfloat16, 128, False),
                (torch.float32, 128, False), (torch.float16, 128, True),
                (torch.bfloat16, 128, True)]
