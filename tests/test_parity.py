@@ -395,3 +395,42 @@ def test_head_dims_32_and_96(dtype, D, case):
     _sync_ok()
     check_fwd(prob, o, lse)
     check_bwd(prob, dq, dk, dv)
+
+
+# ------------------------------------------------------ randomized shapes
+
+def _random_cases(n, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for k in range(n):
+        dtype = [torch.float16, torch.bfloat16][k % 2]
+        D = [64, 128][(k // 2) % 2]
+        Hkv = int(rng.choice([1, 2, 4]))
+        Hq = Hkv * int(rng.choice([1, 2, 3]))
+        window = [(-1, 0), (-1, -1), (int(rng.integers(0, 200)), 0),
+                  (int(rng.integers(0, 90)), int(rng.integers(0, 90)))][int(rng.integers(0, 4))]
+        det = bool(rng.integers(0, 2))
+        if k % 3 == 2:   # THD
+            lengths = [int(x) for x in rng.integers(0, 400, size=int(rng.integers(1, 5)))]
+            cases.append(("thd", dict(lengths=lengths, Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, window=window,
+                                      seed=k, dout_seed=k + 100), det))
+        else:
+            B = int(rng.integers(1, 4))
+            Sq = int(rng.integers(1, 520))
+            Skv = Sq if rng.random() < 0.6 else int(rng.integers(1, 520))
+            cases.append(("dense", dict(B=B, S=Sq, H=Hq, D=D, dtype=dtype, window=window, Hkv=Hkv,
+                                        Skv=Skv, seed=k, dout_seed=k + 100), det))
+    return cases
+
+
+@pytest.mark.parametrize("layout,args,det", _random_cases(24))
+def test_randomized_configs(layout, args, det):
+    """Seeded random shapes across dtypes, head dims, layouts, grouped heads,
+    windows and both backward forms, against the oracle."""
+    prob = inputs.varlen(**args) if layout == "thd" else inputs.dense(**args)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
