@@ -325,6 +325,7 @@ def run_ours(args):
     aux = aux_lines(gb, inputs, dev, peaks) if rank == 0 and not args.no_aux else {}
     if rank == 0 and not args.no_aux:
         aux["causal_fwd_bwd_sweep"] = sweep_lines(gb, inputs, dev, peaks["bf16_tflops"])
+        aux.update(workload_lines(gb, inputs, dev, peaks["bf16_tflops"]))
     cpu = cpu_baseline(args) if rank == 0 and ws == 1 and not args.no_cpu else None
 
     if rank != 0:
@@ -358,6 +359,7 @@ def run_ours(args):
         "fwd_ms": round(fwd_mean, 4), "bwd_ms": round(bwd_mean, 4),
         "fwd_tflops": round(f_fwd / (fwd_mean * 1e-3) / 1e12, 2),
         "bwd_tflops": round(f_bwd / (bwd_mean * 1e-3) / 1e12, 2),
+        "bwd_tflops_without_recompute": round(0.8 * f_bwd / (bwd_mean * 1e-3) / 1e12, 2),
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
                      "peak": peak_bf16, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_bf16, 4),
@@ -413,6 +415,93 @@ def sweep_lines(gb, inputs, dev, peak):
                                                  "pct_of_peak": round(100 * tf / peak, 2)}
         del d, o, lse, dq, dk, dv, work
     return res
+
+
+def _time_steps(one, n, flush=None):
+    """Mean ms of ``one()`` over n calls after 3 warm-up calls.  With a flush
+    buffer, the buffer is overwritten before every call (outside the timed
+    events) so that each call starts with a cold L2."""
+    import torch
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    if flush is None:
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(n):
+            one()
+        s1.record()
+        torch.cuda.synchronize()
+        return s0.elapsed_time(s1) / n
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        flush.fill_(1.0)
+        a.record()
+        one()
+        b.record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / n
+
+
+def workload_lines(gb, inputs, dev, peak):
+    """fwd+bwd TFLOP/s on the packed THD workload (16 causal sequences of
+    U[128, 4096] tokens, 32 query heads over 8 KV heads, D=128), on a causal
+    sliding window (1023, 0) over S=16384, and the S=1024 sweep point with
+    the L2 flushed before every step."""
+    import torch
+    out = {}
+
+    def fwd_bwd(d, window, extra):
+        o, lse = gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=window, **extra)
+        dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+        work = torch.empty(gb.attn_bwd_workspace_size(d.q, d.k, scale=d.scale, window=window,
+                                                      **extra), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=window, out=o, lse=lse, **extra)
+
+        def step():
+            fwd()
+            gb.attn_bwd(d.dout, d.q, d.k, d.v, o, lse, scale=d.scale, window=window, dq=dq,
+                        dk=dk, dv=dv, workspace=work, **extra)
+        return fwd, step
+
+    def line(name, fl_fwd, fl_bwd, ms_fwd, ms_step):
+        tf = (fl_fwd + fl_bwd) / (ms_step * 1e-3) / 1e12
+        return {"workload": name, "ms": round(ms_step, 4), "TFLOP/s": round(tf, 1),
+                "pct_of_peak": round(100 * tf / peak, 2), "fwd_ms": round(ms_fwd, 4),
+                "fwd_TFLOP/s": round(fl_fwd / (ms_fwd * 1e-3) / 1e12, 1)}
+
+    d = inputs.varlen().to(dev)
+    lens = (d.cu_seqlens_q[1:] - d.cu_seqlens_q[:-1]).tolist()
+    nvis = sum(L * (L + 1) // 2 for L in lens) * d.Hq
+    extra = dict(cu_seqlens_q=d.cu_seqlens_q, cu_seqlens_kv=d.cu_seqlens_kv,
+                 max_seqlen_q=d.Sq, max_seqlen_kv=d.Skv)
+    fwd, step = fwd_bwd(d, (-1, 0), extra)
+    out["varlen_thd"] = line("bf16 THD causal, %d sequences U[128,4096] (T=%d), Hq=32 Hkv=8 "
+                             "D=128" % (len(lens), sum(lens)), 4.0 * 128 * nvis,
+                             10.0 * 128 * nvis, _time_steps(fwd, 20), _time_steps(step, 20))
+    del d, fwd, step
+
+    B, S, H, D, win = 1, 16384, 16, 128, (1023, 0)
+    d = inputs.dense(B, S, H, D, window=win, seed=3, dout_seed=4).to(dev)
+    fwd, step = fwd_bwd(d, win, {})
+    f_fwd, f_bwd, _ = flops(B, S, H, D, win)
+    out["sliding_window"] = line("bf16 window (1023, 0), B=1 S=16384 H=16 D=128", f_fwd, f_bwd,
+                                 _time_steps(fwd, 20), _time_steps(step, 20))
+    del d, fwd, step
+
+    B, S, H, D = 16, 1024, 16, 128
+    d = inputs.dense(B, S, H, D, seed=3, dout_seed=4).to(dev)
+    fwd, step = fwd_bwd(d, (-1, 0), {})
+    flush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device=dev)
+    f_fwd, f_bwd, _ = flops(B, S, H, D, (-1, 0))
+    out["causal_s1024_l2_flushed"] = line(
+        "bf16 causal B=16 S=1024 H=16 D=128, 256 MB written before every step", f_fwd, f_bwd,
+        _time_steps(fwd, 20, flush), _time_steps(step, 20, flush))
+    del d, fwd, step, flush
+    return out
 
 
 def aux_lines(gb, inputs, dev, peaks):

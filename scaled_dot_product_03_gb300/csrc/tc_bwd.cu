@@ -320,9 +320,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h2 = 0; h2 < 2; ++h2) {
                 uint32_t sr[32];
                 tmem_ld32(tS + 32 * h2, sr);
+                // 16-byte broadcast reads of the LSE (fewer shared memory wavefronts)
+                const float4 *l4 = reinterpret_cast<const float4 *>(lse2 + 32 * h2);
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    p[32 * h2 + c] = ex2(fmaf(__uint_as_float(sr[c]), c2, -lse2[32 * h2 + c]));
+                for (int q = 0; q < 8; ++q) {
+                    const float4 l = l4[q];
+                    p[32 * h2 + 4 * q] = ex2(fmaf(__uint_as_float(sr[4 * q]), c2, -l.x));
+                    p[32 * h2 + 4 * q + 1] = ex2(fmaf(__uint_as_float(sr[4 * q + 1]), c2, -l.y));
+                    p[32 * h2 + 4 * q + 2] = ex2(fmaf(__uint_as_float(sr[4 * q + 2]), c2, -l.z));
+                    p[32 * h2 + 4 * q + 3] = ex2(fmaf(__uint_as_float(sr[4 * q + 3]), c2, -l.w));
+                }
             }
             if (!full) {
                 // queries that see this key: columns [clo, chi) of this half
@@ -348,11 +355,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h2 = 0; h2 < 2; ++h2) {
                 uint32_t dr[32];
                 tmem_ld32(tP + 32 * h2, dr);
+                const float4 *d4 = reinterpret_cast<const float4 *>(dlt + 32 * h2);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int e = 32 * h2 + 2 * c;
-                    pk[16 * h2 + c] = pack2<T>(p[e] * (__uint_as_float(dr[2 * c]) - dlt[e]),
-                                               p[e + 1] * (__uint_as_float(dr[2 * c + 1]) - dlt[e + 1]));
+                for (int q = 0; q < 8; ++q) {
+                    const float4 d = d4[q];
+                    const int e = 32 * h2 + 4 * q;
+                    pk[16 * h2 + 2 * q] = pack2<T>(p[e] * (__uint_as_float(dr[4 * q]) - d.x),
+                                                   p[e + 1] * (__uint_as_float(dr[4 * q + 1]) - d.y));
+                    pk[16 * h2 + 2 * q + 1] = pack2<T>(p[e + 2] * (__uint_as_float(dr[4 * q + 2]) - d.z),
+                                                       p[e + 3] * (__uint_as_float(dr[4 * q + 3]) - d.w));
                 }
             }
             tmem_st32(tP, pk);

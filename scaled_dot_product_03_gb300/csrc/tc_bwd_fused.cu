@@ -326,10 +326,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                               (g.wr < 0 || n0 + BK - 1 <= i0 + g.wr) && (g.wl < 0 || n0 >= i0 + 31 - g.wl);
             float p[32];
             {
+                // LSE of the 32 columns as 16-byte broadcast reads (fewer
+                // shared memory wavefronts)
                 uint32_t sr[32];
                 tmem_ld32(tS, sr);
+                const float4 *l4 = reinterpret_cast<const float4 *>(lse2);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) p[c] = ex2(fmaf(__uint_as_float(sr[c]), c2, -lse2[c]));
+                for (int q = 0; q < 8; ++q) {
+                    const float4 l = l4[q];
+                    p[4 * q] = ex2(fmaf(__uint_as_float(sr[4 * q]), c2, -l.x));
+                    p[4 * q + 1] = ex2(fmaf(__uint_as_float(sr[4 * q + 1]), c2, -l.y));
+                    p[4 * q + 2] = ex2(fmaf(__uint_as_float(sr[4 * q + 2]), c2, -l.z));
+                    p[4 * q + 3] = ex2(fmaf(__uint_as_float(sr[4 * q + 3]), c2, -l.w));
+                }
             }
             if (!full) {
                 // queries that see this key: columns [clo, chi) of this half
@@ -361,10 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 uint32_t dr[32];
                 tmem_ld32(tDP, dr);
+                const float4 *d4 = reinterpret_cast<const float4 *>(dlt);
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    pk[c] = pack2<T>(p[2 * c] * (__uint_as_float(dr[2 * c]) - dlt[2 * c]),
-                                     p[2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - dlt[2 * c + 1]));
+                for (int q = 0; q < 8; ++q) {
+                    const float4 d = d4[q];
+                    pk[2 * q] = pack2<T>(p[4 * q] * (__uint_as_float(dr[4 * q]) - d.x),
+                                         p[4 * q + 1] * (__uint_as_float(dr[4 * q + 1]) - d.y));
+                    pk[2 * q + 1] = pack2<T>(p[4 * q + 2] * (__uint_as_float(dr[4 * q + 2]) - d.z),
+                                             p[4 * q + 3] * (__uint_as_float(dr[4 * q + 3]) - d.w));
+                }
             }
             tmem_st16(tDP, pk);
             const uint32_t dst = sDSrow + (t & 1) * kDSTile;
