@@ -284,18 +284,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             uint32_t sr[BN];
-            tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-            tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+            tmem_ld128(tS, sr);
             // mask only blocks that some row of the tile sees only in part
             const int rlo = tr[i].row0, rhi = tr[i].row0 + tr[i].nrows - 1;
             const bool full = (n0 + BN - 1 < s.Lkv) && (g.wr < 0 || n0 + BN - 1 <= rlo + g.wr) &&
                               (g.wl < 0 || n0 >= rhi - g.wl);
             float mx = -INFINITY;
             if (full) {
+                // four independent chains of three-input maxima
+                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+                for (int c = 0; c < BN; c += 8) {
+                    m0 = max3f(m0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                    m1 = max3f(m1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                    m2 = max3f(m2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                    m3 = max3f(m3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+                }
+                mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
             } else {
                 // keys visible to this row: columns [vlo, vhi) of the block
                 int vlo = 0, vhi = min(BN, s.Lkv - n0);
@@ -316,14 +321,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 resc = true;
             }
             const float mref = m == -INFINITY ? 0.f : m;
-            float rs = 0.f;
+            // scale and subtract two columns per instruction; the row sum in
+            // two packed accumulators (four partial sums)
+            const uint64_t c2x2 = f2pack(c2, c2), mr2 = f2pack(-mref, -mref);
+            uint64_t rsa = 0ull, rsb = 0ull;
 #pragma unroll
             for (int c = 0; c < BN / 2; ++c) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), c2, -mref));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), c2, -mref));
-                rs += p0 + p1;
+                float x0, x1;
+                f2unpack(fma2(f2pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), c2x2, mr2), x0,
+                         x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                if (c & 1)
+                    rsb = add2(rsb, f2pack(p0, p1));
+                else
+                    rsa = add2(rsa, f2pack(p0, p1));
                 sr[c] = pack2<T>(p0, p1);
             }
+            float ra0, ra1;
+            f2unpack(add2(rsa, rsb), ra0, ra1);
+            const float rs = ra0 + ra1;
             l = l * alpha + rs;
             tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
             tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
