@@ -109,6 +109,23 @@ def test_dense_bf16_sweep_d128_sampled(S, det):
     check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
 
 
+@pytest.mark.parametrize("window,det", [((1023, 0), False), ((1023, 0), True), ((255, 255), False)])
+def test_sliding_window_s16384_sampled(window, det):
+    """A local band over a long sequence (B1 S16384 H16 D128, the bench's
+    sliding-window workload, and a two-sided band): most key blocks of a
+    query tile are skipped, the band's edges are masked inside blocks.
+    Sampled rows and keys include the first and last of the sequence."""
+    prob = inputs.dense(1, 16384, 16, 128, window=window, seed=3, dout_seed=4)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
+    _sync_ok()
+    rows = sample_rows(prob, 48, seed=11)
+    check_fwd(prob, o, lse, row_sel=rows)
+    keys = sample_keys(prob, [(0, 0), (0, prob.Hkv - 1)], 24, seed=11)
+    check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
+
+
 @pytest.mark.parametrize("det", [False, True])
 def test_varlen_thd_gqa_fwd_bwd_sampled(det):
     prob = inputs.varlen()
