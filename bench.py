@@ -266,9 +266,12 @@ def run_ours(args):
     # (and the loss-side O) back.  As in a training loop that prefetches,
     # the steps are pipelined on three streams over two device buffer sets:
     # step i's copy-in (stream s_in) overlaps step i-1's compute, and its
-    # copy-out (stream s_out) overlaps step i+1's compute; events keep a set
-    # from being refilled before its previous step's compute and copy-out are
-    # done.  Every step's copies lie inside the timed region.
+    # copy-out (stream s_out) overlaps step i+1's compute.  A set's inputs
+    # (q, k, v, dO) are refilled once the compute two steps back has read
+    # them, and its outputs (dq, dk, dv, O) rewritten once that step's
+    # copy-out has read them, so copies in both directions run back to back
+    # and the link sets the pace.  Every step's copies lie inside the timed
+    # region.
     hq = [t.cpu().pin_memory() for t in (prob.q, prob.k, prob.v, prob.dout)]
     h2d = sum(t.numel() * t.element_size() for t in hq)
     sets = []
@@ -282,16 +285,18 @@ def run_ours(args):
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("in", "comp", "out")}
     for n in range(2):
+        ev["comp"][n].record(stream)
         ev["out"][n].record(s_out)
 
     def e2e_step(i):
         b, n = sets[i % 2], i % 2
-        s_in.wait_event(ev["out"][n])          # set n's previous step fully done
+        s_in.wait_event(ev["comp"][n])         # set n's inputs read by step i-2
         with torch.cuda.stream(s_in):
             for src_t, dst_t in zip(hq, (b["q"], b["k"], b["v"], b["dout"])):
                 dst_t.copy_(src_t, non_blocking=True)
         ev["in"][n].record(s_in)
         stream.wait_event(ev["in"][n])
+        stream.wait_event(ev["out"][n])        # set n's outputs copied out by step i-2
         gb.attn_fwd(b["q"], b["k"], b["v"], scale=scale, window=win, out=b["o"], lse=b["lse"])
         gb.attn_bwd(b["dout"], b["q"], b["k"], b["v"], b["o"], b["lse"], scale=scale, window=win,
                     dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=work)
