@@ -174,3 +174,32 @@ def test_partitioned_indices_rejects_bad_args(lib):
     assert f(4096, 1, 18, 4, 0, 4096, None) == _lib.ATTN_ERR_INVALID_ARG   # 18 % 8 != 0
     assert f(None, 1, 16, 2, 0, 4096, None) == _lib.ATTN_ERR_INVALID_ARG   # NULL offsets
     assert f(None, 0, 0, 2, 1, None, None) == _lib.ATTN_OK                 # empty: nothing
+
+
+def test_header_is_c99_and_layout_matches_binding(tmp_path):
+    """The header compiles as plain C99 with warnings as errors, and a C
+    compiler lays attn_params and attn_tensor out exactly as the ctypes
+    binding does (sizes and every field offset)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f[0] for f in _lib.AttnParams._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "gbattn.h"\n'
+        "int main(void) {\n"
+        '    printf("attn_params %zu\\n", sizeof(attn_params));\n'
+        '    printf("attn_tensor %zu %zu\\n", sizeof(attn_tensor), offsetof(attn_tensor, stride));\n'
+        + "".join('    printf("%s %%zu\\n", offsetof(attn_params, %s));\n' % (f, f) for f in fields)
+        + "    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           str(src), "-o", str(exe)])
+    out = dict(line.split(" ", 1) for line in subprocess.check_output([str(exe)], text=True).splitlines())
+    assert int(out["attn_params"]) == ctypes.sizeof(_lib.AttnParams)
+    size_t, stride_off = (int(x) for x in out["attn_tensor"].split())
+    assert size_t == ctypes.sizeof(_lib.AttnTensor) and stride_off == _lib.AttnTensor.stride.offset
+    for f in fields:
+        assert int(out[f]) == getattr(_lib.AttnParams, f).offset, f
