@@ -65,16 +65,22 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_ms=10):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
+        self.marks = {}
+
+    def mark(self, name):
+        """Remembers how many samples had arrived at this point."""
+        self.marks[name] = len(self.lines)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "20"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -109,8 +115,13 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+               "reasons": sorted(reasons), "samples": len(sm),
+               "span": "from the start of the timed region through the per-kernel region and the "
+                       "end-to-end leg, every %d ms" % self.period_ms}
+        if "region1_start" in self.marks and "region1_end" in self.marks:
+            out["samples_in_timed_region"] = self.marks["region1_end"] - self.marks["region1_start"]
+        return out
 
 
 def dist_setup(args, backend="nccl"):
@@ -193,16 +204,21 @@ def run_ours(args):
     torch.cuda.synchronize()
     gb.check_device_error()
     # Timed region 1 (the reported value): K steps bracketed only by two
-    # events, a barrier and a synchronize; nvidia-smi samples the clocks.
+    # events, a barrier and a synchronize.  nvidia-smi samples the clocks from
+    # here through region 2 and the end-to-end leg, so that a short region 1
+    # still has a clock record around it (its own samples are counted apart).
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(local).__enter__()
+    time.sleep(0.05)
     barrier(ws)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        start.record(stream)
-        for i in range(args.steps):
-            step()
-        end.record(stream)
-        torch.cuda.synchronize()
+    clk.mark("region1_start")
+    start.record(stream)
+    for i in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk.mark("region1_end")
     barrier(ws)
     gb.check_device_error()
     ms_total = max_over_ranks(start.elapsed_time(end), ws)
@@ -326,6 +342,7 @@ def run_ours(args):
         # the results are those of the device-resident step
         assert torch.equal(sets[0]["o"], sets[1]["o"]) or args.steps < 2
     e2e_tflops = job_throughput(ws, f_fwd + f_bwd, e2e_ms) if e2e_ms == e2e_ms else None
+    clk.__exit__(None, None, None)
 
     aux = aux_lines(gb, inputs, dev, peaks) if rank == 0 and not args.no_aux else {}
     if rank == 0 and not args.no_aux:
@@ -372,6 +389,8 @@ def run_ours(args):
                      "algorithmic_flops_per_launch": dom_flops},
         "kernels": kernels,
         "clocks": clk.summary(),
+        "ms_per_step_x_sm_ghz": (round(ms_step * clk.summary()["sm_mhz"] / 1000.0, 4)
+                                 if clk.summary()["sm_mhz"] else None),
         "e2e": {"value": None if e2e_tflops is None else round(e2e_tflops, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),

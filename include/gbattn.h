@@ -51,7 +51,8 @@
  * The innermost stride (d) must be 1.  For 16-bit types every other stride
  * and the base pointer must be 16-byte aligned (a tensor-memory-accelerator
  * requirement); otherwise the call fails with ATTN_ERR_UNSUPPORTED rather
- * than copying.
+ * than copying.  So does a stride of 2^40 bytes or more on a dim of extent
+ * above 1 (beyond what a tensor map can step).
  *
  * LSE layout: fp32, contiguous, [B, Hq, Sq] for DENSE4D and [Hq, Tq] for THD.
  *
@@ -59,8 +60,10 @@
  * except the attn_params struct itself (host).  The library allocates
  * nothing, copies no input, and never synchronises the host: each call only
  * enqueues kernels on the given stream (NULL = legacy default stream) and
- * returns.  Inputs must stay valid until that work has run.  Calls are
- * thread-safe; the error string is per host thread.
+ * returns.  The stream must belong to the calling thread's current device
+ * (cudaSetDevice), on which the library launches.  Inputs must stay valid
+ * until that work has run.  Calls are thread-safe; the error string is per
+ * host thread.
  *
  * Errors.  Every entry point returns an attn_status.  On ATTN_ERR_INVALID_ARG
  * and ATTN_ERR_UNSUPPORTED nothing has been enqueued.  ATTN_ERR_CUDA reports
@@ -118,7 +121,10 @@ typedef struct {
                             fp16 / bf16 at 64 and 128; FFMA kernels otherwise) */
     const int32_t *cu_seqlens_q;  /* THD only: device, B + 1 non-decreasing */
     const int32_t *cu_seqlens_kv; /* offsets starting at 0 (NULL for DENSE4D) */
-    int max_seqlen_q;    /* THD only: upper bound of the sequence lengths */
+    int max_seqlen_q;    /* THD only: upper bound of the sequence lengths;
+                            grids are sized from it, so a longer sequence is
+                            left partly unwritten and reported by
+                            attn_check_device_error as ATTN_ERR_INVALID_ARG */
     int max_seqlen_kv;
     float scale;         /* softmax scale, finite and > 0, e.g. 1/sqrt(D) */
     int window_left;     /* -1 = unbounded */
@@ -293,7 +299,10 @@ GBATTN_API int attn_profile_read(float *ms, int *kind, int capacity);
  *     rejected with ATTN_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on each device looks up the device address of the
  *     scratch (with that device current); make that first call before any
- *     stream capture begins.
+ *     stream capture begins.  When CUDA loads modules lazily, that first
+ *     call is also when the scratch is reserved on the device, so a caller
+ *     that must not allocate after its set-up should make one accepted
+ *     call during set-up.
  *   - Every call, on every stream, shares the one scratch array, which keeps
  *     the previous call's contents (each call clears what it needs cleared).
  *     Calls whose work may overlap on the GPU (different streams without
@@ -312,9 +321,12 @@ GBATTN_API attn_status attn_bwd_noalloc(const attn_params *p, attn_tensor q,
 GBATTN_API const char *attn_last_error_string(void);
 
 /*
- * Reads and clears the device error word set by kernel watchdogs on the
- * current device.  Synchronises the given stream first.  Returns ATTN_OK or
- * ATTN_ERR_TIMEOUT (or ATTN_ERR_CUDA if the read itself failed).
+ * Reads and clears the device error word set by kernels on the current
+ * device.  Synchronises the given stream first.  Returns ATTN_OK,
+ * ATTN_ERR_TIMEOUT (a kernel watchdog gave up), ATTN_ERR_INVALID_ARG (a THD
+ * sequence was longer than the call's max_seqlen_q / max_seqlen_kv; the
+ * rows past it were not computed), or ATTN_ERR_CUDA if the read itself
+ * failed.
  */
 GBATTN_API attn_status attn_check_device_error(attn_stream_t stream);
 

@@ -34,6 +34,12 @@ def _stream(t: torch.Tensor):
     return ctypes_void(torch.cuda.current_stream(t.device).cuda_stream)
 
 
+def _device_of(t: torch.Tensor):
+    """Makes the tensor's device current for the call: the library launches
+    on the current device and its stream argument must belong to it."""
+    return torch.cuda.device(t.device)
+
+
 def ctypes_void(x):
     import ctypes
     return ctypes.c_void_p(x)
@@ -121,8 +127,9 @@ def attn_fwd(q, k, v, *, scale=None, window=(-1, -1), cu_seqlens_q=None, cu_seql
     if lse is None:
         lse = torch.empty(_lse_shape(p), dtype=torch.float32, device=q.device)
     lib = _lib.load()
-    _lib.check(lib.attn_fwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
-                            _tensor(out, thd), lse.data_ptr(), _stream(q)))
+    with _device_of(q):
+        _lib.check(lib.attn_fwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                                _tensor(out, thd), lse.data_ptr(), _stream(q)))
     return out, lse
 
 
@@ -162,16 +169,18 @@ def attn_bwd(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1), cu_seqlens
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size())
     if dlse is None:
-        _lib.check(lib.attn_bwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
-                                _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
-                                _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd), *ws,
-                                _stream(q)))
+        with _device_of(q):
+            _lib.check(lib.attn_bwd(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                                    _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
+                                    _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd), *ws,
+                                    _stream(q)))
     else:
         assert dlse.dtype == torch.float32 and dlse.is_contiguous() and dlse.shape == lse.shape
-        _lib.check(lib.attn_bwd_dlse(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
-                                     _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
-                                     dlse.data_ptr(), _tensor(dq, thd), _tensor(dk, thd),
-                                     _tensor(dv, thd), *ws, _stream(q)))
+        with _device_of(q):
+            _lib.check(lib.attn_bwd_dlse(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                                         _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
+                                         dlse.data_ptr(), _tensor(dq, thd), _tensor(dk, thd),
+                                         _tensor(dv, thd), *ws, _stream(q)))
     return dq, dk, dv
 
 
@@ -198,10 +207,11 @@ def attn_bwd_noalloc(dout, q, k, v, out, lse, *, scale=None, window=(-1, -1),
     if dv is None:
         dv = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     lib = _lib.load()
-    _lib.check(lib.attn_bwd_noalloc(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
-                                    _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
-                                    _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd),
-                                    _stream(q)))
+    with _device_of(q):
+        _lib.check(lib.attn_bwd_noalloc(p, _tensor(q, thd), _tensor(k, thd), _tensor(v, thd),
+                                        _tensor(out, thd), _tensor(dout, thd), lse.data_ptr(),
+                                        _tensor(dq, thd), _tensor(dk, thd), _tensor(dv, thd),
+                                        _stream(q)))
     return dq, dk, dv
 
 
@@ -227,9 +237,10 @@ def attn_merge_lse(o1, lse1, o2, lse2, *, out=None, lse_out=None
     if o1.dtype not in _DTYPES:
         raise TypeError("unsupported dtype %s" % o1.dtype)
     lib = _lib.load()
-    _lib.check(lib.attn_merge_lse(_DTYPES[o1.dtype], B, S, H, D, _tensor(views[0], False),
-                                  lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
-                                  _tensor(views[2], False), lse_out.data_ptr(), _stream(o1)))
+    with _device_of(o1):
+        _lib.check(lib.attn_merge_lse(_DTYPES[o1.dtype], B, S, H, D, _tensor(views[0], False),
+                                      lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
+                                      _tensor(views[2], False), lse_out.data_ptr(), _stream(o1)))
     return out, lse_out
 
 
@@ -255,12 +266,13 @@ def attn_merge_lse_bwd(o1, lse1, o2, lse2, dout, dlse=None, *, do1=None, dlse1=N
     if o1.dtype not in _DTYPES:
         raise TypeError("unsupported dtype %s" % o1.dtype)
     lib = _lib.load()
-    _lib.check(lib.attn_merge_lse_bwd(_DTYPES[o1.dtype], B, S, H, D, _tensor(views[0], False),
-                                      lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
-                                      _tensor(views[2], False),
-                                      None if dlse is None else dlse.data_ptr(),
-                                      _tensor(views[3], False), dlse1.data_ptr(),
-                                      _tensor(views[4], False), dlse2.data_ptr(), _stream(o1)))
+    with _device_of(o1):
+        _lib.check(lib.attn_merge_lse_bwd(_DTYPES[o1.dtype], B, S, H, D, _tensor(views[0], False),
+                                          lse1.data_ptr(), _tensor(views[1], False), lse2.data_ptr(),
+                                          _tensor(views[2], False),
+                                          None if dlse is None else dlse.data_ptr(),
+                                          _tensor(views[3], False), dlse1.data_ptr(),
+                                          _tensor(views[4], False), dlse2.data_ptr(), _stream(o1)))
     return do1, dlse1, do2, dlse2
 
 

@@ -10,6 +10,7 @@
 #include "launch.h"
 #include "prof.h"
 #include "tc.h"
+#include "tmap.h"
 #include <vector>
 
 namespace gbattn {
@@ -28,6 +29,8 @@ attn_status fail(attn_status st, const char *fmt, ...) {
 }
 
 attn_status cuda_fail(cudaError_t e, const char *what) {
+    if (e == kTmapRefused)  // a view the tensor-memory accelerator cannot address
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: tensor map refused: %s", what, tmap_refusal());
     return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
@@ -96,7 +99,14 @@ attn_status check_params(const attn_params *p) {
     return ATTN_OK;
 }
 
-attn_status check_tensor(const attn_params *p, const attn_tensor &t, const char *name) {
+// Largest byte stride a tensor map can step (the tensor-memory accelerator
+// holds strides in 40 bits).
+constexpr int64_t kMaxTmaStride = (int64_t)1 << 40;
+
+// Checks a view.  rows / heads: extents of its sequence and head dims (the
+// batch dim has B); a dim of extent 1 is never stepped, so its stride is
+// not checked against the accelerator's limits.
+attn_status check_tensor(const attn_params *p, const attn_tensor &t, const char *name, int rows, int heads) {
     if (!t.ptr) return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", name);
     if (t.stride[3] != 1)
         return fail(ATTN_ERR_UNSUPPORTED, "%s: innermost (d) stride %lld must be 1", name,
@@ -108,11 +118,18 @@ attn_status check_tensor(const attn_params *p, const attn_tensor &t, const char 
         const size_t es = elt_size(p->dtype);
         if ((uintptr_t)t.ptr % 16)
             return fail(ATTN_ERR_UNSUPPORTED, "%s: base pointer not 16-byte aligned", name);
-        for (int i = first; i < 3; ++i)
+        const int extent[3] = {p->B, rows, heads};
+        for (int i = first; i < 3; ++i) {
+            if (extent[i] <= 1) continue;
             if ((t.stride[i] * (int64_t)es) % 16)
                 return fail(ATTN_ERR_UNSUPPORTED,
                             "%s: stride[%d]=%lld elements is not a multiple of 16 bytes", name, i,
                             (long long)t.stride[i]);
+            if (t.stride[i] >= kMaxTmaStride / (int64_t)es)
+                return fail(ATTN_ERR_UNSUPPORTED,
+                            "%s: stride[%d]=%lld elements is 2^40 bytes or more, beyond what a "
+                            "tensor map can step", name, i, (long long)t.stride[i]);
+        }
     } else if ((uintptr_t)t.ptr % 4) {
         return fail(ATTN_ERR_UNSUPPORTED, "%s: base pointer not 4-byte aligned", name);
     }
@@ -251,6 +268,10 @@ attn_status attn_check_device_error(attn_stream_t stream) {
         const unsigned zero = 0;
         e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+        if (v & (kErrSeqlenQ | kErrSeqlenKv))
+            return fail(ATTN_ERR_INVALID_ARG,
+                        "a THD sequence is longer than max_seqlen_%s: rows past that length were not "
+                        "computed (code 0x%x)", (v & kErrSeqlenQ) ? "q" : "kv", v);
         return fail(ATTN_ERR_TIMEOUT, "a device-side wait gave up (code 0x%x)", v);
     }
     return ATTN_OK;
@@ -262,8 +283,9 @@ attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     attn_status st = check_params(p);
     if (st != ATTN_OK) return st;
     if (p->B == 0 || max_lq(p) == 0) return ATTN_OK;  // no query row: nothing to write
-    if ((st = check_tensor(p, q, "q")) || (st = check_tensor(p, k, "k")) ||
-        (st = check_tensor(p, v, "v")) || (st = check_tensor(p, o, "o")))
+    const int rq = p->Sq, rkv = p->Skv;
+    if ((st = check_tensor(p, q, "q", rq, p->Hq)) || (st = check_tensor(p, k, "k", rkv, p->Hkv)) ||
+        (st = check_tensor(p, v, "v", rkv, p->Hkv)) || (st = check_tensor(p, o, "o", rq, p->Hq)))
         return st;
     if (!lse) return fail(ATTN_ERR_INVALID_ARG, "lse: NULL pointer");
     FwdArgs a;
@@ -302,10 +324,11 @@ attn_status bwd_impl(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     if (st != ATTN_OK) return st;
     // Nothing to write when there is neither a query row (dq) nor a key row (dk, dv).
     if (p->B == 0 || (max_lq(p) == 0 && max_lkv(p) == 0)) return ATTN_OK;
-    if ((st = check_tensor(p, q, "q")) || (st = check_tensor(p, k, "k")) ||
-        (st = check_tensor(p, v, "v")) || (st = check_tensor(p, o, "o")) ||
-        (st = check_tensor(p, dout, "dout")) || (st = check_tensor(p, dq, "dq")) ||
-        (st = check_tensor(p, dk, "dk")) || (st = check_tensor(p, dv, "dv")))
+    const int rq = p->Sq, rkv = p->Skv;
+    if ((st = check_tensor(p, q, "q", rq, p->Hq)) || (st = check_tensor(p, k, "k", rkv, p->Hkv)) ||
+        (st = check_tensor(p, v, "v", rkv, p->Hkv)) || (st = check_tensor(p, o, "o", rq, p->Hq)) ||
+        (st = check_tensor(p, dout, "dout", rq, p->Hq)) || (st = check_tensor(p, dq, "dq", rq, p->Hq)) ||
+        (st = check_tensor(p, dk, "dk", rkv, p->Hkv)) || (st = check_tensor(p, dv, "dv", rkv, p->Hkv)))
         return st;
     if (!lse) return fail(ATTN_ERR_INVALID_ARG, "lse: NULL pointer");
     const WsLayout w = ws_layout(p);
@@ -331,14 +354,15 @@ attn_status bwd_impl(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     a.watchdog_ns = watchdog_ns();
     if ((st = device_error_word(&a.err))) return st;
     const cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = launch_bwd_preprocess(p->dtype, a, (int)q_rows(p), s);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd preprocess launch");
+    // each launcher encodes its tensor maps before its first launch (the
+    // row-term preprocess), so a refused view enqueues nothing
+    cudaError_t e;
     if (w.fused)
-        e = launch_tc_bwd_fused(p->dtype, a, max_lkv(p), s);
+        e = launch_tc_bwd_fused(p->dtype, a, max_lkv(p), (int)q_rows(p), s);
     else if (uses_tc_bwd(p->dtype, p->D))
         e = launch_tc_bwd(p->dtype, a, max_lq(p), max_lkv(p), (int)q_rows(p), s);
     else
-        e = launch_simt_bwd(p->dtype, a, max_lq(p), max_lkv(p), s);
+        e = launch_simt_bwd(p->dtype, a, max_lq(p), max_lkv(p), (int)q_rows(p), s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
     return ATTN_OK;
 }

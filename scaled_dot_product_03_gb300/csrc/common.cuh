@@ -67,6 +67,18 @@ __device__ __forceinline__ int64_t lse_index(const Geometry &g, const SeqInfo &s
                  : ((int64_t)b * g.Hq + h) * g.Sq + i;
 }
 
+// Bits of the device error word other than the watchdog codes (which stay
+// below 2^16).  THD launches size their grids from max_seqlen_q / _kv; a
+// sequence longer than that would be left partly unprocessed, so the CTA of
+// each sequence's last grid tile reports it with one of these bits.
+constexpr unsigned kErrSeqlenQ = 1u << 30;
+constexpr unsigned kErrSeqlenKv = 1u << 29;
+
+__device__ __forceinline__ void report_uncovered(unsigned *err, const Geometry &g, int len, int covered,
+                                                 unsigned bit) {
+    if (g.thd && len > covered) atomicOr(err, bit);
+}
+
 __device__ __forceinline__ bool visible(int i, int j, int Lkv, int wl, int wr) {
     return j >= 0 && j < Lkv && (wl < 0 || j >= i - wl) && (wr < 0 || j <= i + wr);
 }

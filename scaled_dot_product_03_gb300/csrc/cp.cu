@@ -37,8 +37,12 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_partitioned_indices(const int *pad, int B, int world, int rank, int n_out, int *out,
                                        cudaStream_t st) {
     if (n_out <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     int blocks = (n_out + 255) / 256;
-    if (blocks > 152 * 4) blocks = 152 * 4;
+    if (blocks > sms * 4) blocks = sms * 4;  // grid-stride loop beyond four blocks per SM
     partitioned_indices_kernel<<<blocks, 256, 0, st>>>(pad, B, world, rank, n_out, out);
     return cudaGetLastError();
 }

@@ -38,7 +38,8 @@ struct MergeArgs {
 
 // dtype: 0 = fp16, 1 = bf16, 2 = fp32 (same values as attn_dtype).
 cudaError_t launch_simt_fwd(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st);
-cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv,
+// Preprocess (q_rows query rows), then the FFMA dq and dk/dv kernels.
+cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows,
                             cudaStream_t st);
 cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStream_t st);
 cudaError_t launch_merge(int dtype, const MergeArgs &a, cudaStream_t st);

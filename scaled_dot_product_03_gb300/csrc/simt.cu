@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
     const Geometry &g = a.g;
     const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * BM, tid = threadIdx.x;
     const SeqInfo s = seq_info(g, b);
+    if (blockIdx.x == gridDim.x - 1 && tid == 0) report_uncovered(a.err, g, s.Lq, gridDim.x * BM, kErrSeqlenQ);
     if (m0 >= s.Lq) return;
     const int hk = h / g.G, i = m0 + tid;
     for (int e = tid; e < BM * D; e += kThreads) {
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(BwdArgs a) {
     const Geometry &g = a.g;
     const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * BM, tid = threadIdx.x;
     const SeqInfo s = seq_info(g, b);
+    if (blockIdx.x == gridDim.x - 1 && tid == 0) report_uncovered(a.err, g, s.Lq, gridDim.x * BM, kErrSeqlenQ);
     if (m0 >= s.Lq) return;
     const int hk = h / g.G, i = m0 + tid;
     for (int e = tid; e < BM * D; e += kThreads) {
@@ -271,6 +273,8 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(BwdArgs a) {
     const Geometry &g = a.g;
     const int b = blockIdx.z, hk = blockIdx.y, n0 = blockIdx.x * BN, tid = threadIdx.x;
     const SeqInfo s = seq_info(g, b);
+    if (blockIdx.x == gridDim.x - 1 && tid == 0)
+        report_uncovered(a.err, g, s.Lkv, gridDim.x * BN, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
     const int kt = tid / 4, part = tid % 4, j = n0 + kt;
     float kr[DP], vr[DP], dk[DP], dv[DP];
@@ -358,27 +362,34 @@ cudaError_t fwd_typed(const FwdArgs &a, int max_lq, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+cudaError_t preprocess_any(int dtype, const BwdArgs &a, int rows, cudaStream_t st);
+
 template <typename T, int D>
-cudaError_t bwd_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
+cudaError_t bwd_typed(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows, cudaStream_t st) {
+    const size_t smem_dq = sizeof(float) * (2 * D * (kThreads + 1) + 2 * 16 * D);
+    const size_t smem_kv = sizeof(float) * (2 * 32 * D + 2 * 32);
+    auto kq = simt_bwd_dq_kernel<T, D>;
+    auto kkv = simt_bwd_dkdv_kernel<T, D>;
+    // kernel attributes first, so that a refusal enqueues nothing
+    cudaError_t e;
+    if (max_lq > 0 &&
+        (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dq)) != cudaSuccess)
+        return e;
+    if (max_lkv > 0 &&
+        (e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv)) != cudaSuccess)
+        return e;
+    if ((e = preprocess_any(dtype, a, q_rows, st)) != cudaSuccess) return e;
     if (max_lq > 0) {
-        const size_t smem = sizeof(float) * (2 * D * (kThreads + 1) + 2 * 16 * D);
-        auto k = simt_bwd_dq_kernel<T, D>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
         dim3 grid((max_lq + kThreads - 1) / kThreads, a.g.Hq, a.g.B);
         prof_before(st, kProfSimtBwdDq);
-        k<<<grid, kThreads, smem, st>>>(a);
+        kq<<<grid, kThreads, smem_dq, st>>>(a);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (max_lkv > 0) {
-        const size_t smem = sizeof(float) * (2 * 32 * D + 2 * 32);
-        auto k = simt_bwd_dkdv_kernel<T, D>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
         dim3 grid((max_lkv + kThreads / 4 - 1) / (kThreads / 4), a.g.Hkv, a.g.B);
         prof_before(st, kProfSimtBwdDkDv);
-        k<<<grid, kThreads, smem, st>>>(a);
+        kkv<<<grid, kThreads, smem_kv, st>>>(a);
         prof_after(st);
         return cudaGetLastError();
     }
@@ -427,6 +438,12 @@ void preprocess_typed(const BwdArgs &a, int rows, cudaStream_t st) {
 }
 }  // namespace
 
+namespace {
+cudaError_t preprocess_any(int dtype, const BwdArgs &a, int rows, cudaStream_t st) {
+    return launch_bwd_preprocess(dtype, a, rows, st);
+}
+}  // namespace
+
 cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStream_t st) {
     switch (dtype) {
         case 0: preprocess_typed<__half, 8>(a, rows, st); break;
@@ -443,22 +460,22 @@ cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStr
 }
 
 template <int D>
-cudaError_t bwd_dtype(int dtype, const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
+cudaError_t bwd_dtype(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows, cudaStream_t st) {
     switch (dtype) {
-        case 0: return bwd_typed<__half, D>(a, max_lq, max_lkv, st);
-        case 1: return bwd_typed<__nv_bfloat16, D>(a, max_lq, max_lkv, st);
-        case 2: return bwd_typed<float, D>(a, max_lq, max_lkv, st);
+        case 0: return bwd_typed<__half, D>(dtype, a, max_lq, max_lkv, q_rows, st);
+        case 1: return bwd_typed<__nv_bfloat16, D>(dtype, a, max_lq, max_lkv, q_rows, st);
+        case 2: return bwd_typed<float, D>(dtype, a, max_lq, max_lkv, q_rows, st);
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv,
+cudaError_t launch_simt_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows,
                             cudaStream_t st) {
     switch (a.g.D) {
-        case 32: return bwd_dtype<32>(dtype, a, max_lq, max_lkv, st);
-        case 64: return bwd_dtype<64>(dtype, a, max_lq, max_lkv, st);
-        case 96: return bwd_dtype<96>(dtype, a, max_lq, max_lkv, st);
-        case 128: return bwd_dtype<128>(dtype, a, max_lq, max_lkv, st);
+        case 32: return bwd_dtype<32>(dtype, a, max_lq, max_lkv, q_rows, st);
+        case 64: return bwd_dtype<64>(dtype, a, max_lq, max_lkv, q_rows, st);
+        case 96: return bwd_dtype<96>(dtype, a, max_lq, max_lkv, q_rows, st);
+        case 128: return bwd_dtype<128>(dtype, a, max_lq, max_lkv, q_rows, st);
     }
     return cudaErrorInvalidValue;
 }

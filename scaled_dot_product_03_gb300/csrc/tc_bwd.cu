@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BLK;
+    if (kt == n_ktiles - 1 && threadIdx.x == 0) report_uncovered(a.err, g, s.Lkv, n_ktiles * BLK, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
     const int nkeys = min(BLK, s.Lkv - n0);
 
@@ -623,6 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         T *pend_dst = nullptr;
         for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x) {
             const QTile tl = q_tile(g, w, n_mtiles);
+            if (tl.m0 == (n_mtiles - 1) * BLK && threadIdx.x == 0)
+                report_uncovered(a.err, g, tl.s.Lq, n_mtiles * BLK, kErrSeqlenQ);
             if (tl.nrows == 0) continue;
             const int row = tl.m0 + r;
             T *dst = (T *)a.dq.ptr + (int64_t)tl.b * a.dq.sb + (int64_t)(tl.s.q0 + row) * a.dq.ss +
@@ -752,56 +755,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename T, int D>
-cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
+cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, int q_rows, cudaStream_t st) {
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
-    const uint64_t es = 2;
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
     uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
     uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
-    auto strides = [&](const View &v, const uint64_t dims[4], uint64_t out[3]) {
-        const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
-        for (int i = 0; i < 3; ++i)
-            out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
+    auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
+        tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
     uint64_t sq[3], sk[3], sv[3], sd[3];
     strides(a.q, dq, sq);
     strides(a.k, dk, sk);
     strides(a.v, dk, sv);
     strides(a.dout, dq, sd);
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq{}, tk{}, tv{}, tdo{};
     cudaError_t e;
-    if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BLK)) != cudaSuccess) return e;
-    if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BLK)) != cudaSuccess) return e;
-    if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BLK)) != cudaSuccess) return e;
-    if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BLK)) != cudaSuccess) return e;
-    if (max_lkv > 0) {
-        const int smem = KVCfg<D>::kSmemBytes;
-        auto kern = tc_bwd_dkdv_kernel<T, D>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
-            return e;
-        const int n_ktiles = (max_lkv + BLK - 1) / BLK;
-        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
-        if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    // every map and kernel attribute first: a refusal enqueues nothing
+    const bool kv_pass = max_lkv > 0, q_pass = max_lq > 0;
+    if (kv_pass || q_pass) {
+        if (g.Sq > 0) {
+            if ((e = make_tmap_16bit(&tq, a.q.ptr, dt, dq, sq, BLK)) != cudaSuccess) return e;
+            if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BLK)) != cudaSuccess) return e;
+        }
+        if (g.Skv > 0) {
+            if ((e = make_tmap_16bit(&tk, a.k.ptr, dt, dk, sk, BLK)) != cudaSuccess) return e;
+            if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BLK)) != cudaSuccess) return e;
+        }
+    }
+    auto kv_kern = tc_bwd_dkdv_kernel<T, D>;
+    auto q_kern = tc_bwd_dq_kernel<T, D>;
+    if (kv_pass && (e = cudaFuncSetAttribute(kv_kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             KVCfg<D>::kSmemBytes)) != cudaSuccess)
+        return e;
+    if (q_pass && (e = cudaFuncSetAttribute(q_kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            QCfg<D>::kSmemBytes)) != cudaSuccess)
+        return e;
+    const int n_ktiles = (max_lkv + BLK - 1) / BLK;
+    const int64_t kv_grid = (int64_t)n_ktiles * g.Hkv * g.B;
+    const int n_mtiles = (max_lq + BLK - 1) / BLK;
+    const int64_t n_work = (int64_t)n_mtiles * g.Hq * g.B;
+    if (kv_grid > 0x7fffffff || n_work > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) return e;
+    if (kv_pass && kv_grid > 0) {
         prof_before(st, kProfBwdDkDv);
-        kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a, n_ktiles);
+        kv_kern<<<(unsigned)kv_grid, kThreads, KVCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (max_lq > 0) {
-        const int smem = QCfg<D>::kSmemBytes;
-        auto kern = tc_bwd_dq_kernel<T, D>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
-            return e;
-        const int n_mtiles = (max_lq + BLK - 1) / BLK;
-        const int64_t n_work = (int64_t)n_mtiles * g.Hq * g.B;
-        if (n_work > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (q_pass && n_work > 0) {
         // one CTA per work item: the hardware dispatches them in work order as
         // SMs free up, which balances uneven (causal) items better than a
         // fixed assignment of items to resident CTAs
-        const int grid = (int)n_work;
         prof_before(st, kProfBwdDq);
-        kern<<<grid, kThreads, smem, st>>>(tk, tv, a, n_mtiles);
+        q_kern<<<(int)n_work, kThreads, QCfg<D>::kSmemBytes, st>>>(tk, tv, a, n_mtiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -814,12 +821,11 @@ bool uses_tc_bwd(int dtype, int D) { return (dtype == 0 || dtype == 1) && (D == 
 
 cudaError_t launch_tc_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows,
                           cudaStream_t st) {
-    (void)q_rows;
     switch (dtype * 2 + (a.g.D == 128)) {
-        case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, st);
-        case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, st);
-        case 2: return launch_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, st);
-        case 3: return launch_typed<__nv_bfloat16, 128>(a, max_lq, max_lkv, st);
+        case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, q_rows, st);
+        case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, q_rows, st);
+        case 2: return launch_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, q_rows, st);
+        case 3: return launch_typed<__nv_bfloat16, 128>(a, max_lq, max_lkv, q_rows, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BK;
+    if (kt == n_ktiles - 1 && threadIdx.x == 0) report_uncovered(a.err, g, s.Lkv, n_ktiles * BK, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
     const int nkeys = min(BK, s.Lkv - n0);
 
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) tma_store_4d(m, stage + c * BK * 128, c * 64, s.kv0 + n0, hk, cb);
                 bulk_commit();
-                bulk_wait0();  // before the CTA's shared memory goes away
+                bulk_wait_read0();  // the copy has read the staging before the CTA exits
             }
         } else {
             const MutView &ov = half == 0 ? a.dk : a.dv;
@@ -485,8 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_commit();
             }
         }
-        // the reductions must be complete before the CTA's shared memory goes away
-        if (lane == 0) bulk_wait0();
+        // the reductions must have read their boxes before the CTA's shared
+        // memory goes away (their additions complete with the grid)
+        if (lane == 0) bulk_wait_read0();
         __syncwarp();
     }
     tc_fence_before();
@@ -545,17 +547,14 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float
 }
 
 template <typename T>
-cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
+cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st) {
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
-    const uint64_t es = 2;
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
     uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
     uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
     auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
-        const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
-        for (int i = 0; i < 3; ++i)
-            out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
+        tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
     const uint64_t acc_rows = g.thd ? (uint64_t)g.Tq : (uint64_t)g.Sq;
     const uint64_t acc_heads = g.thd ? (uint64_t)g.Hq : (uint64_t)g.B * g.Hq;
@@ -580,6 +579,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
             cudaSuccess)
             return e;
+        if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) return e;
         const int n_ktiles = (max_lkv + BK - 1) / BK;
         const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -587,6 +587,8 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, tgk, tgv, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) {
+        return e;
     }
     return launch_dq_convert(dt, a, st);
 }
@@ -619,14 +621,14 @@ cudaError_t launch_dq_convert(int dtype, const BwdArgs &a, cudaStream_t st) {
 
 bool uses_tc_bwd_fused(int dtype, int D_) { return (dtype == 0 || dtype == 1) && (D_ == 128 || D_ == 64); }
 
-cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, cudaStream_t st) {
+cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st) {
     // callers route problems without query rows to the two-kernel backward
     if (!a.dq_acc || (a.g.thd ? a.g.Tq : a.g.Sq) <= 0) return cudaErrorInvalidValue;
-    if (a.g.D == 64) return launch_tc_bwd_fused64(dtype, a, max_lkv, st);
+    if (a.g.D == 64) return launch_tc_bwd_fused64(dtype, a, max_lkv, q_rows, st);
     if (a.g.D != D) return cudaErrorInvalidValue;
     switch (dtype) {
-        case 0: return launch_typed<__half>(a, max_lkv, st);
-        case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, st);
+        case 0: return launch_typed<__half>(a, max_lkv, q_rows, st);
+        case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, q_rows, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BK;
+    if (kt == n_ktiles - 1 && threadIdx.x == 0) report_uncovered(a.err, g, s.Lkv, n_ktiles * BK, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
     const int nkeys = min(BK, s.Lkv - n0);
 
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp % 4 == 0 && lane == 0) {
                 tma_store_4d(half == 0 ? &tm_dk : &tm_dv, stage, 0, s.kv0 + n0, hk, cb);
                 bulk_commit();
-                bulk_wait0();
+                bulk_wait_read0();  // the copy has read the staging before the CTA exits
             }
         } else if (j < nkeys) {
             const MutView &ov = half == 0 ? a.dk : a.dv;
@@ -435,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_commit();
             }
         }
-        if (lane == 0) bulk_wait0();
+        // the reductions must have read their boxes before the CTA's shared
+        // memory goes away (their additions complete with the grid)
+        if (lane == 0) bulk_wait_read0();
         __syncwarp();
     }
     tc_fence_before();
@@ -448,17 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename T>
-cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
+cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st) {
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
-    const uint64_t es = 2;
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
     uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
     uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
     auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
-        const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
-        for (int i = 0; i < 3; ++i)
-            out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
+        tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
     const uint64_t acc_rows = g.thd ? (uint64_t)g.Tq : (uint64_t)g.Sq;
     const uint64_t acc_heads = g.thd ? (uint64_t)g.Hq : (uint64_t)g.B * g.Hq;
@@ -483,6 +483,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
             cudaSuccess)
             return e;
+        if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) return e;
         const int n_ktiles = (max_lkv + BK - 1) / BK;
         const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -490,17 +491,19 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, cudaStream_t st) {
         kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, tgk, tgv, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) {
+        return e;
     }
     return launch_dq_convert(dt, a, st);
 }
 
 }  // namespace
 
-cudaError_t launch_tc_bwd_fused64(int dtype, const BwdArgs &a, int max_lkv, cudaStream_t st) {
+cudaError_t launch_tc_bwd_fused64(int dtype, const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st) {
     if (a.g.D != D || !a.dq_acc) return cudaErrorInvalidValue;
     switch (dtype) {
-        case 0: return launch_typed<__half>(a, max_lkv, st);
-        case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, st);
+        case 0: return launch_typed<__half>(a, max_lkv, q_rows, st);
+        case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, q_rows, st);
     }
     return cudaErrorInvalidValue;
 }

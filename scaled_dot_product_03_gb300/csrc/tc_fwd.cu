@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hk = h / g.G;
     const SeqInfo s = seq_info(g, b);
     const int m0 = mt * (BM * NQ);
+    if (rank == 0 && threadIdx.x == 0) report_uncovered(a.err, g, s.Lq, n_mtiles * BM * NQ, kErrSeqlenQ);
     if (m0 >= s.Lq) return;
 
     // key range of the CTA and of each tile
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_store_4d(&tm_o, stage + c * BM * 128, c * 64, q_row + i * BM, h, qb);
                 bulk_commit();
-                bulk_wait0();  // before the CTA's shared memory goes away
+                bulk_wait_read0();  // the copy has read the staging before the CTA exits
             }
         } else {
             T *orow = (T *)a.o.ptr + (int64_t)b * a.o.sb + (int64_t)(s.q0 + row) * a.o.ss +
@@ -446,16 +447,12 @@ cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
     CUtensorMap tq, tk, tv, to;
-    const uint64_t es = 2;
     // dims (d, rows, heads, batch); THD: rows = all tokens, one batch
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
     uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
     uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
-    // byte strides of (rows, heads, batch); a size-1 dim may carry any stride
     auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
-        const int64_t el[3] = {v.ss, v.sh, g.thd ? 0 : v.sb};
-        for (int i = 0; i < 3; ++i)
-            out[i] = (dims[i + 1] == 1 && el[i] == 0) ? 16 : (uint64_t)el[i] * es;
+        tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
     uint64_t sq[3], sk[3], sv[3], so[3];
     strides(a.q, dq, sq);

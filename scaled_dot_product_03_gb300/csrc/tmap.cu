@@ -2,7 +2,9 @@
 // link-time dependency on libcuda).
 #include <cudaTypedefs.h>
 
+#include <cstdio>
 #include <mutex>
+#include <string>
 
 #include "tmap.h"
 
@@ -23,7 +25,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+thread_local std::string t_refusal;
+
+cudaError_t refused(CUresult r, int rank, const cuuint64_t *dims, const cuuint64_t *strides) {
+    char buf[256];
+    int n = snprintf(buf, sizeof buf, "driver error %d for dims (", (int)r);
+    for (int i = 0; i < rank; ++i) n += snprintf(buf + n, sizeof buf - n, i ? ", %llu" : "%llu", (unsigned long long)dims[i]);
+    n += snprintf(buf + n, sizeof buf - n, "), byte strides (");
+    for (int i = 0; i + 1 < rank; ++i)
+        n += snprintf(buf + n, sizeof buf - n, i ? ", %llu" : "%llu", (unsigned long long)strides[i]);
+    snprintf(buf + n, sizeof buf - n, ")");
+    t_refusal = buf;
+    return kTmapRefused;
+}
+
 }  // namespace
+
+const char *tmap_refusal() { return t_refusal.c_str(); }
 
 cudaError_t make_tmap_16bit(CUtensorMap *map, const void *ptr, int dtype, const uint64_t dims[4],
                             const uint64_t strides_bytes[3], uint32_t box_rows) {
@@ -37,7 +55,7 @@ cudaError_t make_tmap_16bit(CUtensorMap *map, const void *ptr, int dtype, const 
                     4, const_cast<void *>(ptr), gdim, gstride, box, estride,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return r == CUDA_SUCCESS ? cudaSuccess : refused(r, 4, gdim, gstride);
 }
 
 cudaError_t make_tmap_f32_acc(CUtensorMap *map, void *ptr, uint64_t cols, uint64_t rows, uint64_t heads,
@@ -52,7 +70,7 @@ cudaError_t make_tmap_f32_acc(CUtensorMap *map, void *ptr, uint64_t cols, uint64
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, gdim, gstride, box, estride,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return r == CUDA_SUCCESS ? cudaSuccess : refused(r, 3, gdim, gstride);
 }
 
 }  // namespace gbattn

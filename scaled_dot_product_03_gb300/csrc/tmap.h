@@ -7,6 +7,21 @@
 
 namespace gbattn {
 
+// Returned by the encoders below when the driver refuses a tensor map (the
+// reason is kept for tmap_refusal()).  No launch path returns this code.
+constexpr cudaError_t kTmapRefused = cudaErrorInvalidPitchValue;
+// The calling thread's last refused encoding: dims and byte strides.
+const char *tmap_refusal();
+
+// Byte strides of the (rows, heads, batch) dims of a view of 2-byte
+// elements, for a tensor map of extents dims (d, rows, heads, batch): a dim
+// of extent 1 is never stepped, so it gets the smallest legal stride (16)
+// whatever the caller's stride for it is.
+inline void tmap_strides(int64_t ss, int64_t sh, int64_t sb, const uint64_t dims[4], uint64_t out[3]) {
+    const int64_t el[3] = {ss, sh, sb};
+    for (int i = 0; i < 3; ++i) out[i] = dims[i + 1] == 1 ? 16 : (uint64_t)el[i] * 2;
+}
+
 // 4-D tiled tensor map over a (d, s, h, b) view of 16-bit elements
 // (dtype 0 = fp16, 1 = bf16), 128-byte swizzle, box {64, box_rows, 1, 1}.
 // dims are element counts innermost first, strides_bytes are the byte

@@ -10,7 +10,11 @@ import scaled_dot_product_03_gb300 as gb
 from helpers import lse_to_library_layout, oracle_bwd, oracle_fwd, to_f64
 
 O_TOL = {torch.float16: 5e-3, torch.bfloat16: 1e-2, torch.float32: 1e-4}
-LSE_TOL = {torch.float16: 1e-3, torch.bfloat16: 1e-3, torch.float32: 1e-3}
+LSE_TOL = {torch.float16: 1e-3, torch.bfloat16: 1e-3}
+# fp32 LSE: 1e-4 plus the rounding of an fp32 number of the LSE's size
+# (scores of magnitude ~200 on the page-3 workload make fp32 rounding alone
+# reach ~1.4e-4 there), per element
+LSE_F32_ABS, LSE_F32_REL = 1e-4, 2.0 ** -20
 GRAD_REL = 2e-2
 # Gradients that are exactly zero (a row that sees a single key has dS = 0)
 # are compared against this floor of max|grad| instead of 0.
@@ -71,9 +75,16 @@ def check_fwd(prob, o, lse, row_sel=None, o_tol=None, lse_tol=None):
     e_o = max_abs(go, ro, full)
     e_l = max_abs(gl, rl, full)
     o_tol = O_TOL[prob.dtype] if o_tol is None else o_tol
-    lse_tol = LSE_TOL[prob.dtype] if lse_tol is None else lse_tol
     assert e_o <= o_tol, "O max-abs error %.3g > %.3g" % (e_o, o_tol)
-    assert e_l <= lse_tol, "LSE max-abs error %.3g > %.3g" % (e_l, lse_tol)
+    if lse_tol is None and prob.dtype == torch.float32:
+        with np.errstate(invalid="ignore"):
+            d = np.abs(gl - rl)[full]
+            bound = LSE_F32_ABS + LSE_F32_REL * np.abs(rl[full])
+        worst = float((d - bound).max()) if d.size else -1.0
+        assert worst <= 0, "fp32 LSE error exceeds 1e-4 + 2^-20 |LSE| by %.3g" % worst
+    else:
+        lse_tol = LSE_TOL[prob.dtype] if lse_tol is None else lse_tol
+        assert e_l <= lse_tol, "LSE max-abs error %.3g > %.3g" % (e_l, lse_tol)
     return e_o, e_l
 
 

@@ -203,3 +203,43 @@ def test_header_is_c99_and_layout_matches_binding(tmp_path):
     assert size_t == ctypes.sizeof(_lib.AttnTensor) and stride_off == _lib.AttnTensor.stride.offset
     for f in fields:
         assert int(out[f]) == getattr(_lib.AttnParams, f).offset, f
+
+
+def test_noalloc_refuses_problems_larger_than_its_scratch(lib):
+    """attn_bwd_noalloc refuses a problem whose workspace would not fit the
+    library's fixed scratch before it touches any device state, so this runs
+    without a GPU (the pointers are never dereferenced)."""
+    p = _lib.AttnParams()
+    p.dtype, p.layout = _lib.ATTN_BF16, _lib.ATTN_LAYOUT_DENSE4D
+    # 64 x 65536 rows x 16 heads of fp32 row terms: 256 MiB of scratch
+    p.B, p.Sq, p.Skv, p.Hq, p.Hkv, p.D = 64, 65536, 65536, 16, 16, 128
+    p.scale, p.window_left, p.window_right = 0.125, -1, 0
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) > _lib.NOALLOC_SCRATCH_BYTES
+    t = _t(strides=(65536 * 2048, 2048, 128, 1))
+    st = lib.attn_bwd_noalloc(ctypes.byref(p), t, t, t, t, t, 4096, t, t, t, None)
+    assert st == _lib.ATTN_ERR_UNSUPPORTED
+    assert b"scratch" in lib.attn_last_error_string()
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_strides_beyond_tensor_map_reach_rejected(lib, which):
+    """A stride of 2^40 bytes or more cannot be stepped by a tensor map: the
+    call fails with UNSUPPORTED before anything is enqueued (forward and
+    backward alike), while the same stride on a dim of extent 1 is never
+    stepped and is accepted by the checks."""
+    big = (1 << 40) // 2  # elements of 2 bytes
+    strides = [32768, 256, 64, 1]
+    strides[which] = big
+    bad = _t(strides=tuple(strides))
+    p = _params()
+    st = lib.attn_fwd(ctypes.byref(p), bad, _t(), _t(), _t(), 4096, None)
+    assert st == _lib.ATTN_ERR_UNSUPPORTED, lib.attn_last_error_string()
+    assert b"2^40" in lib.attn_last_error_string()
+    t = _t()
+    st = lib.attn_bwd(ctypes.byref(p), t, t, t, t, t, 4096, t, t, bad, 4096, 1 << 30, None)
+    assert st == _lib.ATTN_ERR_UNSUPPORTED, lib.attn_last_error_string()
+    # extent-1 dims: B = 1 makes stride[0] irrelevant
+    if which == 0:
+        p1 = _params(B=1)
+        st = lib.attn_fwd(ctypes.byref(p1), bad, bad, bad, bad, 0, None)
+        assert st == _lib.ATTN_ERR_INVALID_ARG  # only the NULL lse is left to reject

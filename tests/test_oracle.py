@@ -493,6 +493,22 @@ def test_partitioned_indices_cover_and_balance(world):
     assert len(set(work)) == 1, work
 
 
+def test_partitioned_indices_within_rank_order_table():
+    """The rows each rank holds, in order, written out by hand for two ranks
+    and three sequences padded to 8, 4 and 12 rows: every sequence is cut
+    into four equal chunks; rank r lists, sequence by sequence, its chunk r
+    and then the mirrored chunk 3 - r (the reading of the THD+CP thread's
+    load-balanced split used throughout)."""
+    pads = [0, 8, 12, 24]
+    want = {
+        0: [0, 1, 6, 7, 8, 11, 12, 13, 14, 21, 22, 23],
+        1: [2, 3, 4, 5, 9, 10, 15, 16, 17, 18, 19, 20],
+    }
+    for rank, rows in want.items():
+        got = oracle.thd_partitioned_indices(pads, 24, 2, rank)
+        assert got.tolist() == rows, (rank, got.tolist())
+
+
 @pytest.mark.parametrize("cp", [2, 3])
 @pytest.mark.parametrize("causal", [True, False])
 def test_ring_attention_equals_full_attention(cp, causal):

@@ -327,6 +327,55 @@ def test_watchdog_gives_up_and_reports():
     check_fwd(prob, o, lse)
 
 
+# ----------------------------------------------- reported argument errors
+
+@pytest.mark.parametrize("which,det", [("q", False), ("kv", False), ("kv", True), ("q", True)])
+def test_thd_understated_max_seqlen_is_reported(which, det):
+    """THD grids are sized from max_seqlen_q / max_seqlen_kv.  A call that
+    understates one of them (here 200 for sequences of 300 and 517 rows)
+    cannot cover the longer sequences; the kernel of each sequence's last
+    grid tile reports that, and attn_check_device_error returns
+    INVALID_ARG.  Every address still comes from cu_seqlens, so the call
+    reads and writes only inside the tensors.  The forward misses query rows
+    (max_seqlen_q); the backward misses key tiles (max_seqlen_kv), and its
+    two-kernel form also query rows."""
+    prob = inputs.varlen(lengths=[300, 64, 517], Hq=4, Hkv=2, D=128, seed=71, dout_seed=72)
+    d = _dev(prob)
+    good = kw(d)
+    bad = dict(good, **{"max_seqlen_" + which: 200})
+    if which == "q":
+        gb.attn_fwd(d.q, d.k, d.v, **bad)
+    else:
+        o, lse = gb.attn_fwd(d.q, d.k, d.v, **good)
+        _sync_ok()
+        gb.attn_bwd(d.dout, d.q, d.k, d.v, o, lse, deterministic=det, **bad)
+    torch.cuda.synchronize()
+    with pytest.raises(gb.AttnError) as ei:
+        gb.check_device_error()
+    assert ei.value.status == 1, str(ei.value)
+    assert "max_seqlen_" + which in str(ei.value)
+    gb.check_device_error()  # cleared
+    o, lse = run_fwd(d)      # and the next correct call is unaffected
+    _sync_ok()
+    check_fwd(prob, o, lse)
+
+
+def test_calls_on_a_non_default_current_stream():
+    """The binding launches on torch's current stream of the tensors'
+    device, here a side stream."""
+    prob = inputs.dense(2, 300, 4, 128, Hkv=2, seed=61, dout_seed=62)
+    d = _dev(prob)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        o, lse = run_fwd(d)
+        dq, dk, dv = run_bwd(d, o, lse)
+    side.synchronize()
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
+
+
 # ------------------------------------------------------- padded cu_seqlens
 
 @pytest.mark.parametrize("dtype,D,det", [(torch.bfloat16, 128, False), (torch.bfloat16, 128, True),
