@@ -151,7 +151,12 @@ GBATTN_API attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor
  * fp32 row terms delta_i = <dO_i, O_i> (one per query row and head) and,
  * when the single-pass backward applies (deterministic == 0, fp16 / bf16,
  * D = 64 or 128, at least one query row), an fp32 dq accumulator of D
- * floats per query row and head.  Returns 0 for invalid parameters.
+ * floats per query row and head.  With grouped heads on a small grid (fewer
+ * than 304 units of 128 keys x key/value head x sequence, fp16 / bf16, D = 64
+ * or 128) the query heads of each group are split over several CTAs, and
+ * the workspace also holds every split's fp32 partial dK and dV (2 D floats
+ * per key row and key/value head per split), summed in split order, so dK and
+ * dV stay reproducible.  Returns 0 for invalid parameters.
  */
 GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
 
@@ -275,7 +280,8 @@ enum {
     ATTN_KERNEL_SIMT_BWD_DKDV = 7,  /* fp32 dK, dV */
     ATTN_KERNEL_BWD_FUSED = 8,      /* tensor-core single-pass dK, dV, dQ share */
     ATTN_KERNEL_BWD_DQ_CONVERT = 9, /* fp32 dq accumulator -> dq */
-    ATTN_KERNEL_MERGE_BWD = 10      /* backward of the LSE merge */
+    ATTN_KERNEL_MERGE_BWD = 10,     /* backward of the LSE merge */
+    ATTN_KERNEL_BWD_DKV_REDUCE = 11 /* dK, dV summed over split query heads */
 };
 GBATTN_API attn_status attn_profile_begin(int max_launches);
 GBATTN_API int attn_profile_read(float *ms, int *kind, int capacity);

@@ -26,7 +26,7 @@ EXPORTS = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_merge_lse",
            "attn_thd_partitioned_indices")
 KERNEL_KINDS = {0: "fwd", 1: "bwd_preprocess", 2: "bwd_dkdv", 3: "bwd_dq", 4: "merge",
                 5: "simt_fwd", 6: "simt_bwd_dq", 7: "simt_bwd_dkdv", 8: "bwd_fused",
-                9: "bwd_dq_convert", 10: "merge_bwd"}
+                9: "bwd_dq_convert", 10: "merge_bwd", 11: "bwd_dkv_reduce"}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI (include/gbattn.h): argument validation, workspace
 // layout, kernel selection by element type, and the device error word.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -190,21 +191,55 @@ bool fused_bwd(const attn_params *p) {
     return !p->deterministic && uses_tc_bwd_fused(p->dtype, p->D) && max_lq(p) > 0;
 }
 
+// CTAs below which the single-pass backward splits the query heads of a
+// key/value group over several CTAs per key tile: twice the SM count of a
+// GB300 (152).  A constant rather than the device's count, so that the
+// workspace size and the order of the partial sums depend on the problem
+// alone.
+constexpr int64_t kSplitTargetCtas = 2 * 152;
+
+// Query-head splits per key tile of the tensor-core dK / dV kernels (the
+// single pass and the deterministic two-kernel form): 1 unless the grid of
+// (key tile, key/value head, sequence) units is small and the groups have
+// several query heads (multi- and grouped-query attention with few
+// key/value heads), in which case enough splits to reach the target, with
+// every split non-empty.  The partial dK, dV of the splits are summed in
+// split order, so both forms keep dK and dV reproducible.
+int fused_split(const attn_params *p) {
+    const int G = p->Hq / p->Hkv;
+    if (G == 1 || !uses_tc_bwd(p->dtype, p->D) || max_lq(p) == 0) return 1;
+    const int64_t units = (int64_t)((max_lkv(p) + 127) / 128) * p->Hkv * p->B;
+    if (units <= 0 || units >= kSplitTargetCtas) return 1;
+    const int64_t want = std::min<int64_t>(G, (kSplitTargetCtas + units - 1) / units);
+    const int gs = (int)((G + want - 1) / want);  // query heads per split
+    return (G + gs - 1) / gs;
+}
+
+int64_t kv_rows(const attn_params *p) {
+    return p->layout == ATTN_LAYOUT_THD ? (int64_t)p->Skv : (int64_t)p->B * p->Skv;
+}
+
 struct WsLayout {
-    size_t delta_off, acc_off, total;
+    size_t delta_off, acc_off, part_off, total;
     bool fused;
+    int nsplit;
 };
 
 // Workspace: the fp32 row terms delta_i = <dO_i, O_i>, laid out like LSE,
 // then (single-pass backward only) the fp32 dq accumulator, D floats per
-// LSE entry.
+// LSE entry, then (split query heads only) the fp32 partial dK and dV of
+// every split.
 WsLayout ws_layout(const attn_params *p) {
     WsLayout w;
     const size_t rows = (size_t)q_rows(p) * p->Hq;
     w.fused = fused_bwd(p);
+    w.nsplit = fused_split(p);
     w.delta_off = 0;
     w.acc_off = round_up(sizeof(float) * rows, 256);
-    w.total = w.fused ? w.acc_off + round_up(sizeof(float) * rows * p->D, 256) : w.acc_off;
+    w.part_off = w.fused ? w.acc_off + round_up(sizeof(float) * rows * p->D, 256) : w.acc_off;
+    w.total = w.part_off;
+    if (w.nsplit > 1)
+        w.total += round_up(sizeof(float) * (size_t)w.nsplit * 2 * kv_rows(p) * p->Hkv * p->D, 256);
     return w;
 }
 
@@ -351,6 +386,8 @@ attn_status bwd_impl(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     a.dv = mview_of(p, dv);
     a.delta = (float *)((char *)workspace + w.delta_off);
     a.dq_acc = w.fused ? (float *)((char *)workspace + w.acc_off) : nullptr;
+    a.nsplit = w.nsplit;
+    a.dkv_part = w.nsplit > 1 ? (float *)((char *)workspace + w.part_off) : nullptr;
     a.watchdog_ns = watchdog_ns();
     if ((st = device_error_word(&a.err))) return st;
     const cudaStream_t s = (cudaStream_t)stream;

@@ -60,6 +60,21 @@ __device__ __forceinline__ SeqInfo seq_info(const Geometry &g, int b) {
     return s;
 }
 
+// Whether token row `row` of a THD buffer lies inside a sequence (rows of
+// the tail, or in the gaps of a padded buffer, do not): the last sequence
+// starting at or before the row must still extend over it.
+__device__ __forceinline__ bool thd_row_in_sequence(const int *cu, const int *pad, int B, int row) {
+    if (B <= 0) return false;
+    const int *start = pad ? pad : cu;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (__ldg(start + mid) <= row) lo = mid; else hi = mid - 1;
+    }
+    const int len = __ldg(cu + lo + 1) - __ldg(cu + lo);
+    return row >= __ldg(start + lo) && row < __ldg(start + lo) + len;
+}
+
 // Index of LSE / row-term element of query row i of head h in sequence b.
 __device__ __forceinline__ int64_t lse_index(const Geometry &g, const SeqInfo &s,
                                              int b, int h, int i) {

@@ -24,6 +24,10 @@ struct BwdArgs {
     float *dq_acc;        // fp32 dq accumulator laid out like LSE with D columns
                           // per row, cleared by the preprocess kernel; null when
                           // the backward does not use one
+    float *dkv_part = nullptr;  // single pass with the query heads of a group split
+                          // over nsplit CTAs: fp32 partial dK, dV per split,
+                          // [nsplit][2][key rows][Hkv][D] (null: no split)
+    int nsplit = 1;       // query-head splits per key tile (1: none)
     unsigned *err;
     uint64_t watchdog_ns;
 };

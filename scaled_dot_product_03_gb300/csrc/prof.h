@@ -20,6 +20,7 @@ enum ProfKind {
     kProfBwdFused = 8,
     kProfBwdDqConvert = 9,
     kProfMergeBwd = 10,
+    kProfBwdDkvReduce = 11,
 };
 
 void prof_before(cudaStream_t st, int kind);

@@ -22,6 +22,8 @@ cudaError_t launch_tc_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, 
 cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st);
 // The head-dim-64 form of the single-pass backward.
 cudaError_t launch_tc_bwd_fused64(int dtype, const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st);
+// dk, dv from the fp32 partials of split query heads (a.dkv_part), D = 64 or 128.
+cudaError_t launch_dkv_reduce(int dtype, const BwdArgs &a, cudaStream_t st);
 // dq = scale * accumulator, in dq's element type and strides (D = 64 or 128).
 cudaError_t launch_dq_convert(int dtype, const BwdArgs &a, cudaStream_t st);
 

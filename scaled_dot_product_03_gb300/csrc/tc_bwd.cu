@@ -118,19 +118,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // banded work order; rank 0 = the first key tiles (seen by the most
     // queries when causal)
-    int bh, kt;
-    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B, bh, kt);
+    // (a split of the query heads of a group counts as a head of its own)
+    int bhs, kt;
+    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B * a.nsplit, bhs, kt);
+    const int sp = bhs % a.nsplit, bh = bhs / a.nsplit;
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BLK;
-    if (kt == n_ktiles - 1 && threadIdx.x == 0) report_uncovered(a.err, g, s.Lkv, n_ktiles * BLK, kErrSeqlenKv);
+    if (kt == n_ktiles - 1 && sp == 0 && threadIdx.x == 0)
+        report_uncovered(a.err, g, s.Lkv, n_ktiles * BLK, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
     const int nkeys = min(BLK, s.Lkv - n0);
+    // query heads of this CTA: [h0, h0 + nh) of the group's G
+    const int gs = (g.G + a.nsplit - 1) / a.nsplit;
+    const int h0 = hk * g.G + sp * gs;
+    const int nh = min(gs, g.G - sp * gs);
 
     int ilo, ihi;
     query_range(n0, n0 + nkeys, s.Lq, g.wl, g.wr, ilo, ihi);
     const int nqb = (ihi - ilo + BLK - 1) / BLK;  // query blocks per head
-    const int n_it = nqb * g.G;
+    const int n_it = nqb * nh;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < n_it; ++t) {
                 const int st = t % QS;
                 const uint32_t ph = (t / QS) & 1;
-                const int h = hk * g.G + t / nqb;
+                const int h = h0 + t / nqb;
                 const int i0 = ilo + (t % nqb) * BLK;
                 // LSE (log2 units) and delta of the block's rows, fetched while
                 // the stage is still in use
@@ -379,6 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         T *dst = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss + (int64_t)hk * ov.sh;
         const float mul = half == 0 ? g.scale : 1.f;
         const uint32_t base = tmem + (half == 0 ? C::kTmDK : C::kTmDV) + lane_off;
+        // split query heads: this split's fp32 partial row instead, summed in
+        // split order by a second kernel
+        float *part = nullptr;
+        if (a.dkv_part) {
+            const int64_t krow = (g.thd ? 0 : (int64_t)b * g.Skv) + s.kv0 + key;
+            const int64_t nrows = g.thd ? g.Skv : (int64_t)g.B * g.Skv;
+            part = a.dkv_part + (((int64_t)(sp * 2 + half) * nrows + krow) * g.Hkv + hk) * D;
+        }
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t v[32];
@@ -388,7 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0u;
             }
-            if (j < nkeys) store_row32<T>(dst + cc * 32, v, mul);
+            if (j < nkeys) {
+                if (part) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(part + cc * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) d4[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                } else {
+                    store_row32<T>(dst + cc * 32, v, mul);
+                }
+            }
         }
     }
     tc_fence_before();
@@ -792,7 +815,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, int q_rows, 
                                             QCfg<D>::kSmemBytes)) != cudaSuccess)
         return e;
     const int n_ktiles = (max_lkv + BLK - 1) / BLK;
-    const int64_t kv_grid = (int64_t)n_ktiles * g.Hkv * g.B;
+    const int64_t kv_grid = (int64_t)n_ktiles * g.Hkv * g.B * a.nsplit;
     const int n_mtiles = (max_lq + BLK - 1) / BLK;
     const int64_t n_work = (int64_t)n_mtiles * g.Hq * g.B;
     if (kv_grid > 0x7fffffff || n_work > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -802,6 +825,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, int q_rows, 
         kv_kern<<<(unsigned)kv_grid, kThreads, KVCfg<D>::kSmemBytes, st>>>(tq, tk, tv, tdo, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (a.dkv_part && (e = launch_dkv_reduce(dt, a, st)) != cudaSuccess) return e;
     }
     if (q_pass && n_work > 0) {
         // one CTA per work item: the hardware dispatches them in work order as

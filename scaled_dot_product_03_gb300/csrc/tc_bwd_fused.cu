@@ -109,19 +109,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // banded work order; rank 0 = the first key tiles (seen by the most
     // queries when causal)
-    int bh, kt;
-    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B, bh, kt, kFusedHeadBand);
+    // (a split of the query heads of a group counts as a head of its own; the
+    // splits of one key/value head are neighbours in the order)
+    int bhs, kt;
+    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B * a.nsplit, bhs, kt, kFusedHeadBand);
+    const int sp = bhs % a.nsplit, bh = bhs / a.nsplit;
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BK;
-    if (kt == n_ktiles - 1 && threadIdx.x == 0) report_uncovered(a.err, g, s.Lkv, n_ktiles * BK, kErrSeqlenKv);
+    if (kt == n_ktiles - 1 && sp == 0 && threadIdx.x == 0)
+        report_uncovered(a.err, g, s.Lkv, n_ktiles * BK, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
     const int nkeys = min(BK, s.Lkv - n0);
+    // query heads of this CTA: [h0, h0 + nh) of the group's G
+    const int gs = (g.G + a.nsplit - 1) / a.nsplit;
+    const int h0 = hk * g.G + sp * gs;
+    const int nh = min(gs, g.G - sp * gs);
 
     int ilo, ihi;
     query_range(n0, n0 + nkeys, s.Lq, g.wl, g.wr, ilo, ihi);
     const int nqb = (ihi - ilo + BQ - 1) / BQ;  // query blocks per head
-    const int n_it = nqb * g.G;
+    const int n_it = nqb * nh;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -173,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < n_it; ++t) {
                 const int st = t % QS;
                 const uint32_t ph = (t / QS) & 1;
-                const int h = hk * g.G + t / nqb;
+                const int h = h0 + t / nqb;
                 const int i0 = ilo + (t % nqb) * BQ;
                 // LSE (log2 units) and delta of the block's rows, fetched while
                 // the stage is still in use
@@ -401,8 +409,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile there (same 128B-swizzled layout as the loads) and write it
         // with TMA stores, which drop rows past a dense tensor's end.  A THD
         // tile that ends inside the tensor would spill into the next
-        // sequence, so it is written row by row instead.
-        if (!g.thd || nkeys == BK) {
+        // sequence, so it is written row by row instead.  With split query
+        // heads the row is this split's fp32 partial, summed by a second
+        // kernel.
+        if (a.dkv_part) {
+            const int64_t krow = (g.thd ? 0 : (int64_t)b * g.Skv) + s.kv0 + key;
+            const int64_t nrows = g.thd ? g.Skv : (int64_t)g.B * g.Skv;
+            float *dst = a.dkv_part + (((int64_t)(sp * 2 + half) * nrows + krow) * g.Hkv + hk) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t v[32];
+                if (n_it > 0) {
+                    tmem_ld32(base + cc * 32, v);  // warp-wide: every lane loads
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (j < nkeys) store_f32_row32(dst + cc * 32, v);
+            }
+        } else if (!g.thd || nkeys == BK) {
             uint8_t *stage = smem + (half == 0 ? kKOff : kVOff);
             const uint32_t srow = smem_u32(stage) + j * 128;
 #pragma unroll
@@ -459,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int zb = g.thd ? 0 : b * g.Hq;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
-            const int h = hk * g.G + t / nqb;
+            const int h = h0 + t / nqb;
             const int i0 = ilo + (t % nqb) * BQ;
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.dq_full, t & 1, wd, 0xf0));
             if (!ok) break;
@@ -518,16 +543,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float
             srow = (int)(r % g.Tq);
             b = 0;
             // token rows outside every sequence (the tail, or the gaps of a
-            // padded buffer) are not written: find the last sequence that
-            // starts at or before the row
-            const int *start = g.pad_q ? g.pad_q : g.cu_q;
-            int lo = 0, hi = g.B - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) / 2;
-                if (__ldg(start + mid) <= srow) lo = mid; else hi = mid - 1;
-            }
-            const int len = __ldg(g.cu_q + lo + 1) - __ldg(g.cu_q + lo);
-            if (g.B <= 0 || srow < __ldg(start + lo) || srow >= __ldg(start + lo) + len) continue;
+            // padded buffer) are not written
+            if (!thd_row_in_sequence(g.cu_q, g.pad_q, g.B, srow)) continue;
         } else {
             const int64_t bhr = r / g.Sq;
             srow = (int)(r % g.Sq);
@@ -543,6 +560,59 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float
         y.w = pack2<T>(x1.z * g.scale, x1.w * g.scale);
         T *dst = (T *)dq.ptr + (int64_t)b * dq.sb + (int64_t)srow * dq.ss + (int64_t)h * dq.sh + c * 8;
         *reinterpret_cast<uint4 *>(dst) = y;
+    }
+}
+
+// Split query heads: dk = scale * (sum of the splits' partial dK) and
+// dv = sum of their partial dV, added in split order (so the result does not
+// depend on scheduling) and written in the element type and strides of dk,
+// dv.  Partials: [nsplit][2][rows][Hkv][DD] fp32.  8 head dims per thread.
+template <typename T, int DD>
+__global__ void __launch_bounds__(256)
+    dkv_reduce_kernel(MutView dk, MutView dv, const float *__restrict__ part, int nsplit, Geometry g) {
+    constexpr int C = DD / 8;
+    const int64_t rows = g.thd ? (int64_t)g.Skv : (int64_t)g.B * g.Skv;
+    const int64_t slice = rows * g.Hkv * DD;  // floats of one (split, dK or dV)
+    const int64_t n = rows * g.Hkv * C;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(idx % C);
+        const int64_t rh = idx / C;  // (row, head)
+        const int hk = (int)(rh % g.Hkv);
+        const int64_t r = rh / g.Hkv;
+        int b = 0, key = (int)r;
+        if (g.thd) {
+            if (!thd_row_in_sequence(g.cu_kv, g.pad_kv, g.B, key)) continue;
+        } else {
+            b = (int)(r / g.Skv);
+            key = (int)(r % g.Skv);
+        }
+        float sk[8], sv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sk[e] = sv[e] = 0.f;
+        const float *src = part + rh * DD + c * 8;
+        for (int sp = 0; sp < nsplit; ++sp) {
+            const float4 *pk = reinterpret_cast<const float4 *>(src + (int64_t)(2 * sp) * slice);
+            const float4 *pv = reinterpret_cast<const float4 *>(src + (int64_t)(2 * sp + 1) * slice);
+            const float4 k0 = __ldg(pk), k1 = __ldg(pk + 1), v0 = __ldg(pv), v1 = __ldg(pv + 1);
+            sk[0] += k0.x; sk[1] += k0.y; sk[2] += k0.z; sk[3] += k0.w;
+            sk[4] += k1.x; sk[5] += k1.y; sk[6] += k1.z; sk[7] += k1.w;
+            sv[0] += v0.x; sv[1] += v0.y; sv[2] += v0.z; sv[3] += v0.w;
+            sv[4] += v1.x; sv[5] += v1.y; sv[6] += v1.z; sv[7] += v1.w;
+        }
+        uint4 yk, yv;
+        yk.x = pack2<T>(sk[0] * g.scale, sk[1] * g.scale);
+        yk.y = pack2<T>(sk[2] * g.scale, sk[3] * g.scale);
+        yk.z = pack2<T>(sk[4] * g.scale, sk[5] * g.scale);
+        yk.w = pack2<T>(sk[6] * g.scale, sk[7] * g.scale);
+        yv.x = pack2<T>(sv[0], sv[1]);
+        yv.y = pack2<T>(sv[2], sv[3]);
+        yv.z = pack2<T>(sv[4], sv[5]);
+        yv.w = pack2<T>(sv[6], sv[7]);
+        const int64_t ok = (int64_t)b * dk.sb + (int64_t)key * dk.ss + (int64_t)hk * dk.sh + c * 8;
+        const int64_t ov = (int64_t)b * dv.sb + (int64_t)key * dv.ss + (int64_t)hk * dv.sh + c * 8;
+        *reinterpret_cast<uint4 *>((T *)dk.ptr + ok) = yk;
+        *reinterpret_cast<uint4 *>((T *)dv.ptr + ov) = yv;
     }
 }
 
@@ -581,16 +651,31 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
             return e;
         if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) return e;
         const int n_ktiles = (max_lkv + BK - 1) / BK;
-        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
+        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B * a.nsplit;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdFused);
         kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, tgk, tgv, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (a.dkv_part && (e = launch_dkv_reduce(dt, a, st)) != cudaSuccess) return e;
     } else if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) {
         return e;
     }
     return launch_dq_convert(dt, a, st);
+}
+
+template <typename T, int DD>
+cudaError_t dkv_reduce_typed(const BwdArgs &a, cudaStream_t st) {
+    const Geometry &g = a.g;
+    const int64_t rows = g.thd ? (int64_t)g.Skv : (int64_t)g.B * g.Skv;
+    const int64_t n = rows * g.Hkv * (DD / 8);
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks <= 0) return cudaSuccess;
+    prof_before(st, kProfBwdDkvReduce);
+    dkv_reduce_kernel<T, DD><<<(unsigned)blocks, 256, 0, st>>>(a.dk, a.dv, a.dkv_part, a.nsplit, g);
+    prof_after(st);
+    return cudaGetLastError();
 }
 
 template <typename T, int DD>
@@ -615,6 +700,16 @@ cudaError_t launch_dq_convert(int dtype, const BwdArgs &a, cudaStream_t st) {
         case 1: return dq_convert_typed<__half, 128>(a, st);
         case 2: return dq_convert_typed<__nv_bfloat16, 64>(a, st);
         case 3: return dq_convert_typed<__nv_bfloat16, 128>(a, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dkv_reduce(int dtype, const BwdArgs &a, cudaStream_t st) {
+    switch (dtype * 2 + (a.g.D == 128)) {
+        case 0: return dkv_reduce_typed<__half, 64>(a, st);
+        case 1: return dkv_reduce_typed<__half, 128>(a, st);
+        case 2: return dkv_reduce_typed<__nv_bfloat16, 64>(a, st);
+        case 3: return dkv_reduce_typed<__nv_bfloat16, 128>(a, st);
     }
     return cudaErrorInvalidValue;
 }

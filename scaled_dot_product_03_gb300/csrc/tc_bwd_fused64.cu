@@ -96,19 +96,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *s_delta = s_lse + QS * BQ;
     const Geometry &g = a.g;
 
-    int bh, kt;
-    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B, bh, kt, kHeadBand);
+    // (a split of the query heads of a group counts as a head of its own; the
+    // splits of one key/value head are neighbours in the order)
+    int bhs, kt;
+    banded_order(blockIdx.x, n_ktiles, g.Hkv * g.B * a.nsplit, bhs, kt, kHeadBand);
+    const int sp = bhs % a.nsplit, bh = bhs / a.nsplit;
     const int hk = bh % g.Hkv, b = bh / g.Hkv;
     const SeqInfo s = seq_info(g, b);
     const int n0 = kt * BK;
-    if (kt == n_ktiles - 1 && threadIdx.x == 0) report_uncovered(a.err, g, s.Lkv, n_ktiles * BK, kErrSeqlenKv);
+    if (kt == n_ktiles - 1 && sp == 0 && threadIdx.x == 0)
+        report_uncovered(a.err, g, s.Lkv, n_ktiles * BK, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
     const int nkeys = min(BK, s.Lkv - n0);
+    // query heads of this CTA: [h0, h0 + nh) of the group's G
+    const int gs = (g.G + a.nsplit - 1) / a.nsplit;
+    const int h0 = hk * g.G + sp * gs;
+    const int nh = min(gs, g.G - sp * gs);
 
     int ilo, ihi;
     query_range(n0, n0 + nkeys, s.Lq, g.wl, g.wr, ilo, ihi);
     const int nqb = (ihi - ilo + BQ - 1) / BQ;
-    const int n_it = nqb * g.G;
+    const int n_it = nqb * nh;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < n_it; ++t) {
                 const int st = t % QS;
                 const uint32_t ph = (t / QS) & 1;
-                const int h = hk * g.G + t / nqb;
+                const int h = h0 + t / nqb;
                 const int i0 = ilo + (t % nqb) * BQ;
                 float lv[4], dv[4];
 #pragma unroll
@@ -376,7 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; ++e) v[32 * cc + e] = 0u;
             }
         }
-        if (!g.thd || nkeys == BK) {
+        if (a.dkv_part) {
+            // split query heads: this split's fp32 partial row, summed by a
+            // second kernel
+            if (j < nkeys) {
+                const int64_t krow = (g.thd ? 0 : (int64_t)b * g.Skv) + s.kv0 + key;
+                const int64_t nrows = g.thd ? g.Skv : (int64_t)g.B * g.Skv;
+                float *dst = a.dkv_part + (((int64_t)(sp * 2 + half) * nrows + krow) * g.Hkv + hk) * D;
+                store_f32_row32(dst, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                store_f32_row32(dst + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            }
+        } else if (!g.thd || nkeys == BK) {
             uint8_t *stage = smem + (half == 0 ? kKOff : kVOff);
             const uint32_t srow = smem_u32(stage) + j * 128;
 #pragma unroll
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int zb = g.thd ? 0 : b * g.Hq;
         bool ok = true;
         for (int t = 0; t < n_it; ++t) {
-            const int h = hk * g.G + t / nqb;
+            const int h = h0 + t / nqb;
             const int i0 = ilo + (t % nqb) * BQ;
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.dq_full, t & 1, wd, 0xf8));
             if (!ok) break;
@@ -485,12 +503,13 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
             return e;
         if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) return e;
         const int n_ktiles = (max_lkv + BK - 1) / BK;
-        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B;
+        const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B * a.nsplit;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdFused);
         kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, tgk, tgv, a, n_ktiles);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (a.dkv_part && (e = launch_dkv_reduce(dt, a, st)) != cudaSuccess) return e;
     } else if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) {
         return e;
     }

@@ -58,5 +58,12 @@ __device__ __forceinline__ void store_row32(T *dst, const uint32_t (&v)[32], flo
     for (int e = 0; e < 4; ++e) d4[e] = pk[e];
 }
 
+// Writes 32 fp32 values of one row (16-byte stores).
+__device__ __forceinline__ void store_f32_row32(float *dst, const uint32_t (&v)[32]) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) d4[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+}
+
 }  // namespace tcu
 }  // namespace gbattn

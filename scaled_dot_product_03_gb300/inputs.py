@@ -149,12 +149,15 @@ def pr1(seed: int = 0) -> Attn:
 
 
 def page1(scale: float = 1.0, seed: int = 0, seqlen: int = 2048,
-          q_heads: int = 16, kv_heads: int = 1, head_dim: int = 64) -> Attn:
+          q_heads: int = 16, kv_heads: int = 1, head_dim: int = 64,
+          dout_seed: Optional[int] = None) -> Attn:
     """Packed ``qkv[s, 1, h + 2 h_g, d]`` split on dim 2 into q, k, v views.
 
     The views are sbhd tensors; they are exposed in (b, s, h, d) order by a
     permute, which changes no memory, so their element strides are
-    (b, s, h, d) = (1152, 1152, 64, 1) at the page's sizes.
+    (b, s, h, d) = (1152, 1152, 64, 1) at the page's sizes.  With
+    ``dout_seed`` an upstream gradient ``[1, s, h, d]`` (contiguous) is drawn
+    from its own generator for the backward.
     """
     g = _gen(seed)
     H = q_heads + 2 * kv_heads
@@ -167,9 +170,14 @@ def page1(scale: float = 1.0, seed: int = 0, seqlen: int = 2048,
         "v": ("qkv", (1, seqlen, kv_heads, head_dim), bstride,
               (q_heads + kv_heads) * head_dim),
     }
+    bases = {"qkv": qkv}
+    if dout_seed is not None:
+        dout = _randn((1, seqlen, q_heads, head_dim), _gen(dout_seed), torch.float16)
+        bases["dout"] = dout
+        views["dout"] = ("dout", tuple(dout.shape), tuple(dout.stride()), 0)
     return Attn("page1_fp16_packed_sbhd_s%d_scale%g" % (seqlen, scale),
                 torch.float16, "dense", 1, seqlen, seqlen, q_heads, kv_heads,
-                head_dim, float(scale), (-1, 0), {"qkv": qkv}, views)
+                head_dim, float(scale), (-1, 0), bases, views)
 
 
 def page3(seed: int = 0) -> Attn:

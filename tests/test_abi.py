@@ -123,13 +123,23 @@ def test_workspace_size(lib):
     p32 = _params(dtype=_lib.ATTN_F32)
     assert lib.attn_bwd_workspace_size(ctypes.byref(p32)) >= 4 * rows * p.Hq
     # 16-bit, D = 128: the single pass adds an fp32 dq accumulator, the
-    # deterministic form needs the row terms only
+    # deterministic form needs the row terms only (one query head per
+    # key/value head: no query-head split)
     for dt in (_lib.ATTN_F16, _lib.ATTN_BF16):
-        pf = _params(dtype=dt, D=128)
+        pf = _params(dtype=dt, D=128, Hkv=4)
         assert lib.attn_bwd_workspace_size(ctypes.byref(pf)) >= 4 * rows * pf.Hq * (1 + 128)
         pf.deterministic = 1
         nd = lib.attn_bwd_workspace_size(ctypes.byref(pf))
         assert 4 * rows * pf.Hq <= nd < 4 * rows * pf.Hq + 256
+    # grouped heads on a small grid (2 key tiles x 2 key/value heads x 2
+    # sequences): the query heads of a group are split in two, and both
+    # backward forms add the fp32 partial dK, dV of each split
+    for det in (0, 1):
+        pg = _params(D=128, Hq=4, Hkv=2, deterministic=det)
+        n = lib.attn_bwd_workspace_size(ctypes.byref(pg))
+        parts = 2 * 2 * (pg.B * pg.Skv) * pg.Hkv * 128 * 4
+        base = 4 * rows * pg.Hq * (1 if det else 1 + 128)
+        assert base + parts <= n < base + parts + 512, (det, n)
     pf = _params(dtype=_lib.ATTN_BF16, D=128)
     pf.deterministic = 2
     assert lib.attn_bwd_workspace_size(ctypes.byref(pf)) == 0

@@ -48,6 +48,51 @@ def test_page1_packed_views_equal_contiguous_and_oracle(scale):
     check_fwd(prob, o, lse)
 
 
+@pytest.mark.parametrize("scale,det", [(1.0, False), (0.1, False), (0.1, True)])
+def test_page1_mqa_backward_full_size_sampled(scale, det):
+    """The page-1 workload (fp16, S=2048, 16 query heads over one KV head,
+    packed strided views) through the backward at full size: the single pass
+    splits the 16 query heads of the group over CTAs and sums their fp32
+    dK / dV partials.  Sampled rows (dq) and keys (dk, dv, which sum over all
+    16 heads) against the oracle."""
+    prob = inputs.page1(scale=scale, dout_seed=5)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
+    _sync_ok()
+    rows = sample_rows(prob, 48, seed=7)
+    check_fwd(prob, o, lse, row_sel=rows)
+    keys = sample_keys(prob, [(0, 0)], 64, seed=7)
+    check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
+
+
+def test_mqa_d128_backward_sampled():
+    """Multi-query attention at head dim 128 (16 query heads over one KV
+    head, B=2, S=4096): the query-head split of the single pass at D=128."""
+    prob = inputs.dense(2, 4096, 16, 128, Hkv=1, seed=13, dout_seed=14)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    rows = sample_rows(prob, 24, seed=13)
+    check_fwd(prob, o, lse, row_sel=rows)
+    keys = sample_keys(prob, [(0, 0), (1, 0)], 24, seed=13)
+    check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
+
+
+def test_split_and_unsplit_backward_agree_bitwise_on_dkdv():
+    """dK and dV of the split single pass are sums of per-split partials in a
+    fixed order, so repeated runs give bitwise equal dK and dV."""
+    prob = inputs.dense(1, 1000, 8, 64, Hkv=1, seed=17, dout_seed=18)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    a = run_bwd(d, o, lse)
+    b = run_bwd(d, o, lse)
+    _sync_ok()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    check_bwd(prob, *a)
+
+
 def test_page3_fp32_forward_backward():
     prob = inputs.page3()
     d = _dev(prob)
