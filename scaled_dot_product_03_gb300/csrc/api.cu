@@ -245,6 +245,24 @@ WsLayout ws_layout(const attn_params *p) {
 
 }  // namespace
 
+cudaError_t device_sm_count(int *out) {
+    static std::mutex mu;
+    static int counts[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!counts[dev]) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        counts[dev] = n > 0 ? n : 1;
+    }
+    *out = counts[dev];
+    return cudaSuccess;
+}
+
 // ----------------------------------------------------------------- timing
 // Per-thread launch timing: while enabled, each kernel launch is bracketed
 // by two events recorded on its stream.

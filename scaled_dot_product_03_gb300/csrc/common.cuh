@@ -134,6 +134,33 @@ __device__ __forceinline__ void banded_order(int w, int nt, int nbh, int &bh, in
     bh = h0 + r % bs;
 }
 
+// Unsigned 32-bit division by a divisor fixed for a launch, as a multiply
+// and shifts (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, the round-up method for N-bit unsigned operands):
+// with 2^(l-1) < d <= 2^l and m = floor(2^32 (2^l - d) / d) + 1,
+//   t = umulhi(m, n),  n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0)
+// for every 32-bit n.  Built on the host, used by the streaming kernels whose
+// per-row index arithmetic would otherwise be dominated by divisions.
+struct FastDiv {
+    uint32_t d, m, s1, s2;
+    FastDiv() = default;
+    __host__ explicit FastDiv(uint32_t div) : d(div) {
+        uint32_t l = 0;
+        while (l < 32 && ((uint64_t)1 << l) < div) ++l;
+        m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << l) - div)) / div + 1);
+        s1 = l < 1 ? l : 1;
+        s2 = l > 0 ? l - 1 : 0;
+    }
+    __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+        const uint32_t t = __umulhi(m, n);
+#else
+        const uint32_t t = (uint32_t)(((uint64_t)m * n) >> 32);
+#endif
+        return (t + ((n - t) >> s1)) >> s2;
+    }
+};
+
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }

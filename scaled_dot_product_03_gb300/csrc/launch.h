@@ -40,6 +40,9 @@ struct MergeArgs {
     float *lse_out;
 };
 
+// Streaming multiprocessors of the current device (queried once per device).
+cudaError_t device_sm_count(int *out);
+
 // dtype: 0 = fp16, 1 = bf16, 2 = fp32 (same values as attn_dtype).
 cudaError_t launch_simt_fwd(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st);
 // Preprocess (q_rows query rows), then the FFMA dq and dk/dv kernels.

@@ -179,6 +179,71 @@ __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
     }
 }
 
+// The same for 16-bit O and dO with the head dim fixed at compile time: a
+// row is covered by LPR lanes moving one 16-byte vector of O and of dO each
+// (LPR = D / 8 rounded up to a power of two; the spare lanes of D = 96 idle),
+// and every warp keeps U row groups in flight before it reduces any, so each
+// lane has U pairs of loads outstanding.  Index arithmetic is 32-bit (the
+// launcher guarantees fewer than 2^31 (row, head) pairs).
+template <typename T, int D, int U>
+__global__ void __launch_bounds__(256) bwd_preprocess16_kernel(BwdArgs a, int rows, FastDiv fHq, FastDiv fSq) {
+    constexpr int NV = D / 8;                              // 16-byte vectors per row
+    constexpr int LPR = NV <= 4 ? 4 : NV <= 8 ? 8 : 16;   // lanes per row
+    constexpr int RPW = 32 / LPR;                         // rows per warp and group
+    const Geometry &g = a.g;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
+    const unsigned pairs = (unsigned)rows * (unsigned)g.Hq;
+    const unsigned nwarps = gridDim.x * (blockDim.x / 32);
+    for (unsigned base = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * (RPW * U); base < pairs;
+         base += nwarps * (RPW * U)) {
+        uint4 x[U], y[U];
+        unsigned idx[U];
+        bool act[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const unsigned pr = base + u * RPW + sub;
+            act[u] = pr < pairs;
+            x[u] = y[u] = make_uint4(0, 0, 0, 0);
+            idx[u] = 0;
+            if (act[u]) {
+                const unsigned r = fHq.div(pr), h = pr - r * (unsigned)g.Hq;
+                unsigned b = 0, row = r;
+                if (g.thd) {
+                    idx[u] = h * (unsigned)g.Tq + r;
+                } else {
+                    b = fSq.div(r);
+                    row = r - b * (unsigned)g.Sq;
+                    idx[u] = (b * (unsigned)g.Hq + h) * (unsigned)g.Sq + row;
+                }
+                if (c < NV) {
+                    x[u] = reinterpret_cast<const uint4 *>(row_ptr<T>(a.o, b, row, h))[c];
+                    y[u] = reinterpret_cast<const uint4 *>(row_ptr<T>(a.dout, b, row, h))[c];
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const T *xv = reinterpret_cast<const T *>(&x[u]);
+            const T *yv = reinterpret_cast<const T *>(&y[u]);
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(to_f32(xv[e]), to_f32(yv[e]), acc);
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (act[u]) {
+                if (a.dq_acc && c < NV) {
+                    float4 *z = reinterpret_cast<float4 *>(a.dq_acc + (size_t)idx[u] * D + c * 8);
+                    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                // a gradient reaching LSE adds P_ij dLSE_i to dS_ij, i.e.
+                // lowers the row term by dLSE_i
+                if (c == 0) a.delta[idx[u]] = a.dlse ? acc - a.dlse[idx[u]] : acc;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Backward dq: thread = query row; K, V blocks in shared memory.
 template <typename T, int D>
@@ -444,10 +509,53 @@ cudaError_t preprocess_any(int dtype, const BwdArgs &a, int rows, cudaStream_t s
 }
 }  // namespace
 
+namespace {
+template <typename T, int D>
+cudaError_t preprocess16_typed(const BwdArgs &a, int rows, cudaStream_t st) {
+    constexpr int U = 4;
+    constexpr int NV = D / 8;
+    constexpr int LPR = NV <= 4 ? 4 : NV <= 8 ? 8 : 16;
+    const int64_t pairs = (int64_t)rows * a.g.Hq;
+    int sms = 0;
+    cudaError_t e = device_sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    // warps needed, U row groups of 32 / LPR rows each; at most 8 blocks of
+    // 256 threads per SM, the rest by the grid-stride loop
+    const int64_t warps = (pairs + (32 / LPR) * U - 1) / ((32 / LPR) * U);
+    int64_t blocks = (warps + 7) / 8;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    if (blocks < 1) blocks = 1;
+    prof_before(st, kProfBwdPreprocess);
+    bwd_preprocess16_kernel<T, D, U><<<(unsigned)blocks, 256, 0, st>>>(a, rows, FastDiv(a.g.Hq),
+                                                                       FastDiv(a.g.Sq > 0 ? a.g.Sq : 1));
+    prof_after(st);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t preprocess16_any(const BwdArgs &a, int rows, cudaStream_t st) {
+    switch (a.g.D) {
+        case 32: return preprocess16_typed<T, 32>(a, rows, st);
+        case 64: return preprocess16_typed<T, 64>(a, rows, st);
+        case 96: return preprocess16_typed<T, 96>(a, rows, st);
+        case 128: return preprocess16_typed<T, 128>(a, rows, st);
+    }
+    return cudaErrorInvalidValue;
+}
+}  // namespace
+
 cudaError_t launch_bwd_preprocess(int dtype, const BwdArgs &a, int rows, cudaStream_t st) {
+    // 32-bit index arithmetic in the 16-bit kernel
+    const bool idx32 = (int64_t)rows * a.g.Hq < ((int64_t)1 << 31);
     switch (dtype) {
-        case 0: preprocess_typed<__half, 8>(a, rows, st); break;
-        case 1: preprocess_typed<__nv_bfloat16, 8>(a, rows, st); break;
+        case 0:
+            if (idx32) return preprocess16_any<__half>(a, rows, st);
+            preprocess_typed<__half, 8>(a, rows, st);
+            break;
+        case 1:
+            if (idx32) return preprocess16_any<__nv_bfloat16>(a, rows, st);
+            preprocess_typed<__nv_bfloat16, 8>(a, rows, st);
+            break;
         case 2:
             if (rows_aligned16(a.o, 4) && rows_aligned16(a.dout, 4))
                 preprocess_typed<float, 4>(a, rows, st);

@@ -525,75 +525,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// dq = scale * acc in the element type, acc laid out like LSE with D columns
-// per row.  8 head dims per thread (two 16-byte loads, one 16-byte store).
-template <typename T, int DD>
-__global__ void __launch_bounds__(256) dq_convert_kernel(MutView dq, const float *__restrict__ acc, Geometry g) {
-    constexpr int C = DD / 8;
-    const int64_t rows = g.thd ? (int64_t)g.Hq * g.Tq : (int64_t)g.B * g.Hq * g.Sq;
-    const int64_t n = rows * C;
-
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = idx / C;
-        const int c = (int)(idx % C);
-        int b, h, srow;
-        if (g.thd) {
-            h = (int)(r / g.Tq);
-            srow = (int)(r % g.Tq);
-            b = 0;
-            // token rows outside every sequence (the tail, or the gaps of a
-            // padded buffer) are not written
-            if (!thd_row_in_sequence(g.cu_q, g.pad_q, g.B, srow)) continue;
-        } else {
-            const int64_t bhr = r / g.Sq;
-            srow = (int)(r % g.Sq);
-            b = (int)(bhr / g.Hq);
-            h = (int)(bhr % g.Hq);
+// dq = scale * acc in the element type, acc laid out like LSE with DD
+// columns per row.  A row is covered by DD / 8 lanes, each reading 8 floats
+// (two 16-byte loads) and writing 8 elements (one 16-byte store); every warp
+// keeps U rows per lane group in flight.  32-bit index arithmetic (the
+// launcher guarantees fewer than 2^31 rows).
+template <typename T, int DD, int U>
+__global__ void __launch_bounds__(256)
+    dq_convert_kernel(MutView dq, const float *__restrict__ acc, Geometry g, FastDiv fRows, FastDiv fHq) {
+    constexpr int LPR = DD / 8;
+    constexpr int RPW = 32 / LPR;
+    const unsigned rows = g.thd ? (unsigned)g.Hq * (unsigned)g.Tq : (unsigned)g.B * (unsigned)g.Hq * (unsigned)g.Sq;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
+    const unsigned nwarps = gridDim.x * (blockDim.x / 32);
+    for (unsigned base = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * (RPW * U); base < rows;
+         base += nwarps * (RPW * U)) {
+        float4 x0[U], x1[U];
+        T *dst[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const unsigned r = base + u * RPW + sub;
+            dst[u] = nullptr;
+            if (r >= rows) continue;
+            unsigned b = 0, h, srow;
+            // fRows divides by the rows of one head (Tq for THD, Sq dense)
+            if (g.thd) {
+                h = fRows.div(r);
+                srow = r - h * (unsigned)g.Tq;
+                // token rows outside every sequence (the tail, or the gaps of a
+                // padded buffer) are not written
+                if (!thd_row_in_sequence(g.cu_q, g.pad_q, g.B, (int)srow)) continue;
+            } else {
+                const unsigned bh = fRows.div(r);
+                srow = r - bh * (unsigned)g.Sq;
+                b = fHq.div(bh);
+                h = bh - b * (unsigned)g.Hq;
+            }
+            const float4 *src = reinterpret_cast<const float4 *>(acc + (size_t)r * DD + c * 8);
+            x0[u] = __ldg(src);
+            x1[u] = __ldg(src + 1);
+            dst[u] = (T *)dq.ptr + (int64_t)b * dq.sb + (int64_t)srow * dq.ss + (int64_t)h * dq.sh + c * 8;
         }
-        const float4 *src = reinterpret_cast<const float4 *>(acc + r * DD + c * 8);
-        const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
-        uint4 y;
-        y.x = pack2<T>(x0.x * g.scale, x0.y * g.scale);
-        y.y = pack2<T>(x0.z * g.scale, x0.w * g.scale);
-        y.z = pack2<T>(x1.x * g.scale, x1.y * g.scale);
-        y.w = pack2<T>(x1.z * g.scale, x1.w * g.scale);
-        T *dst = (T *)dq.ptr + (int64_t)b * dq.sb + (int64_t)srow * dq.ss + (int64_t)h * dq.sh + c * 8;
-        *reinterpret_cast<uint4 *>(dst) = y;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (!dst[u]) continue;
+            uint4 y;
+            y.x = pack2<T>(x0[u].x * g.scale, x0[u].y * g.scale);
+            y.y = pack2<T>(x0[u].z * g.scale, x0[u].w * g.scale);
+            y.z = pack2<T>(x1[u].x * g.scale, x1[u].y * g.scale);
+            y.w = pack2<T>(x1[u].z * g.scale, x1[u].w * g.scale);
+            *reinterpret_cast<uint4 *>(dst[u]) = y;
+        }
     }
 }
 
 // Split query heads: dk = scale * (sum of the splits' partial dK) and
 // dv = sum of their partial dV, added in split order (so the result does not
 // depend on scheduling) and written in the element type and strides of dk,
-// dv.  Partials: [nsplit][2][rows][Hkv][DD] fp32.  8 head dims per thread.
+// dv.  Partials: [nsplit][2][rows][Hkv][DD] fp32.  A (row, head) is covered
+// by DD / 8 lanes of 8 head dims each; 32-bit index arithmetic.
 template <typename T, int DD>
 __global__ void __launch_bounds__(256)
     dkv_reduce_kernel(MutView dk, MutView dv, const float *__restrict__ part, int nsplit, Geometry g) {
-    constexpr int C = DD / 8;
-    const int64_t rows = g.thd ? (int64_t)g.Skv : (int64_t)g.B * g.Skv;
-    const int64_t slice = rows * g.Hkv * DD;  // floats of one (split, dK or dV)
-    const int64_t n = rows * g.Hkv * C;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int c = (int)(idx % C);
-        const int64_t rh = idx / C;  // (row, head)
-        const int hk = (int)(rh % g.Hkv);
-        const int64_t r = rh / g.Hkv;
-        int b = 0, key = (int)r;
+    constexpr int LPR = DD / 8;
+    constexpr int RPW = 32 / LPR;
+    const unsigned nrows = g.thd ? (unsigned)g.Skv : (unsigned)g.B * (unsigned)g.Skv;
+    const unsigned pairs = nrows * (unsigned)g.Hkv;
+    const size_t slice = (size_t)pairs * DD;  // floats of one (split, dK or dV)
+    const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
+    const unsigned nwarps = gridDim.x * (blockDim.x / 32);
+    for (unsigned rh = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * RPW + sub; rh < pairs;
+         rh += nwarps * RPW) {
+        const unsigned r = rh / (unsigned)g.Hkv, hk = rh - r * (unsigned)g.Hkv;
+        unsigned b = 0, key = r;
         if (g.thd) {
-            if (!thd_row_in_sequence(g.cu_kv, g.pad_kv, g.B, key)) continue;
+            if (!thd_row_in_sequence(g.cu_kv, g.pad_kv, g.B, (int)key)) continue;
         } else {
-            b = (int)(r / g.Skv);
-            key = (int)(r % g.Skv);
+            b = r / (unsigned)g.Skv;
+            key = r - b * (unsigned)g.Skv;
         }
         float sk[8], sv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) sk[e] = sv[e] = 0.f;
-        const float *src = part + rh * DD + c * 8;
+        const float *src = part + (size_t)rh * DD + c * 8;
         for (int sp = 0; sp < nsplit; ++sp) {
-            const float4 *pk = reinterpret_cast<const float4 *>(src + (int64_t)(2 * sp) * slice);
-            const float4 *pv = reinterpret_cast<const float4 *>(src + (int64_t)(2 * sp + 1) * slice);
+            const float4 *pk = reinterpret_cast<const float4 *>(src + (size_t)(2 * sp) * slice);
+            const float4 *pv = reinterpret_cast<const float4 *>(src + (size_t)(2 * sp + 1) * slice);
             const float4 k0 = __ldg(pk), k1 = __ldg(pk + 1), v0 = __ldg(pv), v1 = __ldg(pv + 1);
             sk[0] += k0.x; sk[1] += k0.y; sk[2] += k0.z; sk[3] += k0.w;
             sk[4] += k1.x; sk[5] += k1.y; sk[6] += k1.z; sk[7] += k1.w;
@@ -667,11 +684,15 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
 template <typename T, int DD>
 cudaError_t dkv_reduce_typed(const BwdArgs &a, cudaStream_t st) {
     const Geometry &g = a.g;
-    const int64_t rows = g.thd ? (int64_t)g.Skv : (int64_t)g.B * g.Skv;
-    const int64_t n = rows * g.Hkv * (DD / 8);
-    int64_t blocks = (n + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
-    if (blocks <= 0) return cudaSuccess;
+    const int64_t pairs = (g.thd ? (int64_t)g.Skv : (int64_t)g.B * g.Skv) * g.Hkv;
+    if (pairs <= 0) return cudaSuccess;
+    if (pairs >= ((int64_t)1 << 31)) return cudaErrorInvalidConfiguration;
+    int sms = 0;
+    cudaError_t e = device_sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    const int64_t warps = (pairs + (256 / DD) - 1) / (256 / DD);
+    int64_t blocks = (warps + 7) / 8;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     prof_before(st, kProfBwdDkvReduce);
     dkv_reduce_kernel<T, DD><<<(unsigned)blocks, 256, 0, st>>>(a.dk, a.dv, a.dkv_part, a.nsplit, g);
     prof_after(st);
@@ -680,14 +701,22 @@ cudaError_t dkv_reduce_typed(const BwdArgs &a, cudaStream_t st) {
 
 template <typename T, int DD>
 cudaError_t dq_convert_typed(const BwdArgs &a, cudaStream_t st) {
+    constexpr int U = 4;
     const Geometry &g = a.g;
     const int64_t rows = g.thd ? (int64_t)g.Hq * g.Tq : (int64_t)g.B * g.Hq * g.Sq;
-    const int64_t n = rows * (DD / 8);
-    int64_t blocks = (n + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
-    if (blocks <= 0) return cudaSuccess;
+    if (rows <= 0) return cudaSuccess;
+    if (rows >= ((int64_t)1 << 31)) return cudaErrorInvalidConfiguration;
+    int sms = 0;
+    cudaError_t e = device_sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    const int64_t per_warp = (32 / (DD / 8)) * U;
+    const int64_t warps = (rows + per_warp - 1) / per_warp;
+    int64_t blocks = (warps + 7) / 8;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     prof_before(st, kProfBwdDqConvert);
-    dq_convert_kernel<T, DD><<<(unsigned)blocks, 256, 0, st>>>(a.dq, a.dq_acc, g);
+    const int per_head = g.thd ? g.Tq : g.Sq;
+    dq_convert_kernel<T, DD, U><<<(unsigned)blocks, 256, 0, st>>>(a.dq, a.dq_acc, g, FastDiv(per_head > 0 ? per_head : 1),
+                                                                  FastDiv(g.Hq));
     prof_after(st);
     return cudaGetLastError();
 }

@@ -290,29 +290,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rlo = tr[i].row0, rhi = tr[i].row0 + tr[i].nrows - 1;
             const bool full = (n0 + BN - 1 < s.Lkv) && (g.wr < 0 || n0 + BN - 1 <= rlo + g.wr) &&
                               (g.wl < 0 || n0 >= rhi - g.wl);
-            float mx = -INFINITY;
-            if (full) {
-                // four independent chains of three-input maxima
-                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < BN; c += 8) {
-                    m0 = max3f(m0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-                    m1 = max3f(m1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-                    m2 = max3f(m2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-                    m3 = max3f(m3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-                }
-                mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-            } else {
+            if (!full) {
                 // keys visible to this row: columns [vlo, vhi) of the block
                 int vlo = 0, vhi = min(BN, s.Lkv - n0);
                 if (g.wl >= 0) vlo = max(vlo, row - g.wl - n0);
                 if (g.wr >= 0) vhi = min(vhi, row + g.wr + 1 - n0);
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
+                for (int c = 0; c < BN; ++c)
                     if (c < vlo || c >= vhi) sr[c] = __float_as_uint(-INFINITY);
-                    mx = fmaxf(mx, __uint_as_float(sr[c]));
-                }
             }
+            // four independent chains of three-input maxima
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; c += 8) {
+                m0 = max3f(m0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                m1 = max3f(m1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                m2 = max3f(m2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                m3 = max3f(m3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+            }
+            const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
             const float xm = mx * c2;  // scale > 0, so the max commutes with scaling
             float alpha = 1.f;
             bool resc = false;
