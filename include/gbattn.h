@@ -118,7 +118,8 @@ typedef struct {
                             Tq and Tkv of the packed q and k/v tensors */
     int Hq, Hkv;         /* query heads, key/value heads (Hq % Hkv == 0) */
     int D;               /* head dimension: 32, 64, 96 or 128 (tensor cores for
-                            fp16 / bf16 at 64 and 128; FFMA kernels otherwise) */
+                            fp16 / bf16, 32 and 96 on the 64- and 128-wide
+                            kernels with zero padding; FFMA kernels for fp32) */
     const int32_t *cu_seqlens_q;  /* THD only: device, B + 1 non-decreasing */
     const int32_t *cu_seqlens_kv; /* offsets starting at 0 (NULL for DENSE4D) */
     int max_seqlen_q;    /* THD only: upper bound of the sequence lengths;
@@ -150,13 +151,14 @@ GBATTN_API attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor
  * Bytes of device scratch memory attn_bwd needs for these parameters: the
  * fp32 row terms delta_i = <dO_i, O_i> (one per query row and head) and,
  * when the single-pass backward applies (deterministic == 0, fp16 / bf16,
- * D = 64 or 128, at least one query row), an fp32 dq accumulator of D
- * floats per query row and head.  With grouped heads on a small grid (fewer
- * than 304 units of 128 keys x key/value head x sequence, fp16 / bf16, D = 64
- * or 128) the query heads of each group are split over several CTAs, and
- * the workspace also holds every split's fp32 partial dK and dV (2 D floats
- * per key row and key/value head per split), summed in split order, so dK and
- * dV stay reproducible.  Returns 0 for invalid parameters.
+ * at least one query row), an fp32 dq accumulator of D' floats per query row
+ * and head, D' = 64 for D <= 64 and 128 otherwise (the head dim the
+ * tensor-core kernels compute with).  With grouped heads on a small grid
+ * (fewer than 304 units of 128 keys x key/value head x sequence, fp16 /
+ * bf16) the query heads of each group are split over several CTAs, and the
+ * workspace also holds every split's fp32 partial dK and dV (2 D' floats per
+ * key row and key/value head per split), summed in split order, so dK and dV
+ * stay reproducible.  Returns 0 for invalid parameters.
  */
 GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
 
@@ -170,12 +172,12 @@ GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
  * o and lse must be the forward's outputs for the same inputs.  dq has q's
  * shape, dk and dv k's shape, each with its own strides (they may be views
  * of one packed gradient buffer).
- * Determinism.  With p->deterministic = 0 and fp16 / bf16 inputs of head
- * dim 64 or 128, one pass over the (key block, query block) pairs forms S and dP
+ * Determinism.  With p->deterministic = 0 and fp16 / bf16 inputs, one pass
+ * over the (key block, query block) pairs forms S and dP
  * once and adds each pair's share of dq into an fp32 accumulator in the
  * workspace; those fp32 additions happen in an order set by the GPU's
  * scheduling, so dq may differ between runs in its last bits (dk and dv do
- * not).  In every other case (p->deterministic = 1, fp32, D = 32 or 96) every
+ * not).  In every other case (p->deterministic = 1, or fp32) every
  * output element is written by exactly one thread of one kernel and the
  * results do not depend on scheduling.  workspace: device memory of at least
  * attn_bwd_workspace_size(p) bytes, 256-byte aligned, whose contents on

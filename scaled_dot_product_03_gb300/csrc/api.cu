@@ -236,10 +236,12 @@ WsLayout ws_layout(const attn_params *p) {
     w.nsplit = fused_split(p);
     w.delta_off = 0;
     w.acc_off = round_up(sizeof(float) * rows, 256);
-    w.part_off = w.fused ? w.acc_off + round_up(sizeof(float) * rows * p->D, 256) : w.acc_off;
+    // (the tensor-core kernels lay out dq sums and partials tc_dim(D) wide)
+    const size_t dc = (size_t)tc_dim(p->D);
+    w.part_off = w.fused ? w.acc_off + round_up(sizeof(float) * rows * dc, 256) : w.acc_off;
     w.total = w.part_off;
     if (w.nsplit > 1)
-        w.total += round_up(sizeof(float) * (size_t)w.nsplit * 2 * kv_rows(p) * p->Hkv * p->D, 256);
+        w.total += round_up(sizeof(float) * (size_t)w.nsplit * 2 * kv_rows(p) * p->Hkv * dc, 256);
     return w;
 }
 
@@ -405,6 +407,7 @@ attn_status bwd_impl(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     a.delta = (float *)((char *)workspace + w.delta_off);
     a.dq_acc = w.fused ? (float *)((char *)workspace + w.acc_off) : nullptr;
     a.nsplit = w.nsplit;
+    a.acc_d = tc_dim(p->D);
     a.dkv_part = w.nsplit > 1 ? (float *)((char *)workspace + w.part_off) : nullptr;
     a.watchdog_ns = watchdog_ns();
     if ((st = device_error_word(&a.err))) return st;

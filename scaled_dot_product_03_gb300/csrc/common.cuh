@@ -38,6 +38,13 @@ struct Geometry {
     float scale_log2;     // scale * log2(e)
 };
 
+// Head dim the tensor-core kernels compute with for a head dim D of 32, 64,
+// 96 or 128: 32 runs on the 64-wide kernels and 96 on the 128-wide ones.
+// Tensor maps keep the real D as their inner extent, so the loads fill the
+// columns past D with zeros (which add nothing to any product) and the
+// stores drop them; row-by-row stores stop at D.
+__host__ __device__ constexpr int tc_dim(int D) { return D <= 64 ? 64 : 128; }
+
 struct SeqInfo {
     int q0, kv0;  // first row of the sequence (THD), 0 for dense
     int Lq, Lkv;  // lengths

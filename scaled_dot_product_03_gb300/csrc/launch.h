@@ -28,6 +28,8 @@ struct BwdArgs {
                           // over nsplit CTAs: fp32 partial dK, dV per split,
                           // [nsplit][2][key rows][Hkv][D] (null: no split)
     int nsplit = 1;       // query-head splits per key tile (1: none)
+    int acc_d = 0;        // floats per row of dq_acc and of the partials (the
+                          // tensor-core head dim, tc_dim(D))
     unsigned *err;
     uint64_t watchdog_ns;
 };

@@ -155,7 +155,9 @@ __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
             }
             const Vt *o = reinterpret_cast<const Vt *>(row_ptr<T>(a.o, b, row, h));
             const Vt *d_o = reinterpret_cast<const Vt *>(row_ptr<T>(a.dout, b, row, h));
-            float *acc_row = a.dq_acc ? a.dq_acc + idx * D : nullptr;
+            // (the accumulator rows are acc_d floats apart; columns past D
+            // are padding that is never read)
+            float *acc_row = a.dq_acc ? a.dq_acc + idx * a.acc_d : nullptr;
             for (int c = c0; c < chunks; c += tpr) {
                 const Vt x = o[c], y = d_o[c];
 #pragma unroll
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess16_kernel(BwdArgs a, int ro
             for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (act[u]) {
                 if (a.dq_acc && c < NV) {
-                    float4 *z = reinterpret_cast<float4 *>(a.dq_acc + (size_t)idx[u] * D + c * 8);
+                    float4 *z = reinterpret_cast<float4 *>(a.dq_acc + (size_t)idx[u] * a.acc_d + c * 8);
                     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
                     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
@@ -463,8 +465,8 @@ cudaError_t bwd_typed(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int 
 
 }  // namespace
 
-// Head dims with a kernel: 64 and 128 (also served by the tensor-core
-// kernels for 16-bit types) and 32, 96 (this path only, for every type).
+// Head dims with a kernel: 32, 64, 96 and 128, for every element type (16-bit
+// types normally take the tensor-core kernels; fp32 always comes here).
 template <int D>
 cudaError_t fwd_dtype(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st) {
     switch (dtype) {

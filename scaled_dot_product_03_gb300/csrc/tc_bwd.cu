@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0u;
             }
-            if (j < nkeys) {
+            if (j < nkeys && (part || cc * 32 < g.D)) {
                 if (part) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(part + cc * 32);
 #pragma unroll
@@ -659,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-                    for (int cc = 0; cc < D / 64; ++cc) store_row32<T>(dst + cc * 32, z, 1.f);
+                    for (int cc = 0; cc < D / 64; ++cc)
+                        if (half * (D / 2) + cc * 32 < g.D) store_row32<T>(dst + cc * 32, z, 1.f);
                 }
                 continue;
             }
@@ -674,9 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[32];
                     uint4 *v4 = reinterpret_cast<uint4 *>(v);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        v4[e] = r < tl.nrows ? reinterpret_cast<const uint4 *>(p + cc * 64)[e]
-                                             : make_uint4(0, 0, 0, 0);
+                    for (int e = 0; e < 8; ++e)  // (columns past the head dim: zero padding)
+                        v4[e] = r < tl.nrows && cc * 64 + e * 8 < g.D ? reinterpret_cast<const uint4 *>(p + cc * 64)[e]
+                                                                       : make_uint4(0, 0, 0, 0);
                     tmem_st32(dstc + cc * 32, v);
                 }
                 tmem_wait_st();
@@ -686,8 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pend_dst) {  // previous item's dq, overlapping this item's first MMAs
 #pragma unroll
                 for (int cc = 0; cc < D / 64; ++cc)
-                    store_row32<T>(pend_dst + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&pend[cc * 32]),
-                                   g.scale);
+                    if (half * (D / 2) + cc * 32 < g.D)
+                        store_row32<T>(pend_dst + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&pend[cc * 32]),
+                                       g.scale);
                 pend_dst = nullptr;
             }
             float lse2 = 0.f, dlt = 0.f;
@@ -765,7 +767,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pend_dst) {
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc)
-                store_row32<T>(pend_dst + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&pend[cc * 32]), g.scale);
+                if (half * (D / 2) + cc * 32 < g.D)
+                    store_row32<T>(pend_dst + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&pend[cc * 32]), g.scale);
         }
     }
     tc_fence_before();
@@ -782,8 +785,9 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, int q_rows, 
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
-    uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
-    uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
+    // inner extent: the real head dim (columns past it load as zeros)
+    uint64_t dq[4] = {(uint64_t)g.D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
+    uint64_t dk[4] = {(uint64_t)g.D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
     auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
         tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
@@ -841,11 +845,13 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lq, int max_lkv, int q_rows, 
 
 }  // namespace
 
-bool uses_tc_bwd(int dtype, int D) { return (dtype == 0 || dtype == 1) && (D == 64 || D == 128); }
+bool uses_tc_bwd(int dtype, int D) {
+    return (dtype == 0 || dtype == 1) && (D == 32 || D == 64 || D == 96 || D == 128);
+}
 
 cudaError_t launch_tc_bwd(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows,
                           cudaStream_t st) {
-    switch (dtype * 2 + (a.g.D == 128)) {
+    switch (dtype * 2 + (tc_dim(a.g.D) == 128)) {
         case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, q_rows, st);
         case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, q_rows, st);
         case 2: return launch_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, q_rows, st);

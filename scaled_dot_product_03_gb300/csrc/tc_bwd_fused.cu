@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0u;
                 }
-                if (j < nkeys) store_row32<T>(dstp + cc * 32, v, mul);
+                if (j < nkeys && cc * 32 < g.D) store_row32<T>(dstp + cc * 32, v, mul);
             }
         }
     } else if (warp >= kDrainWarp0) {
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(256)
         for (int u = 0; u < U; ++u) {
             const unsigned r = base + u * RPW + sub;
             dst[u] = nullptr;
-            if (r >= rows) continue;
+            if (r >= rows || c * 8 >= g.D) continue;  // (columns past the head dim are padding)
             unsigned b = 0, h, srow;
             // fRows divides by the rows of one head (Tq for THD, Sq dense)
             if (g.thd) {
@@ -596,6 +596,7 @@ __global__ void __launch_bounds__(256)
     const unsigned nwarps = gridDim.x * (blockDim.x / 32);
     for (unsigned rh = (blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * RPW + sub; rh < pairs;
          rh += nwarps * RPW) {
+        if (c * 8 >= g.D) continue;  // (columns past the head dim are padding)
         const unsigned r = rh / (unsigned)g.Hkv, hk = rh - r * (unsigned)g.Hkv;
         unsigned b = 0, key = r;
         if (g.thd) {
@@ -638,8 +639,9 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
-    uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
-    uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
+    // inner extent: the real head dim (columns past it load as zeros)
+    uint64_t dq[4] = {(uint64_t)g.D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
+    uint64_t dk[4] = {(uint64_t)g.D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
     auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
         tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
@@ -724,7 +726,7 @@ cudaError_t dq_convert_typed(const BwdArgs &a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_dq_convert(int dtype, const BwdArgs &a, cudaStream_t st) {
-    switch (dtype * 2 + (a.g.D == 128)) {
+    switch (dtype * 2 + (tc_dim(a.g.D) == 128)) {
         case 0: return dq_convert_typed<__half, 64>(a, st);
         case 1: return dq_convert_typed<__half, 128>(a, st);
         case 2: return dq_convert_typed<__nv_bfloat16, 64>(a, st);
@@ -734,7 +736,7 @@ cudaError_t launch_dq_convert(int dtype, const BwdArgs &a, cudaStream_t st) {
 }
 
 cudaError_t launch_dkv_reduce(int dtype, const BwdArgs &a, cudaStream_t st) {
-    switch (dtype * 2 + (a.g.D == 128)) {
+    switch (dtype * 2 + (tc_dim(a.g.D) == 128)) {
         case 0: return dkv_reduce_typed<__half, 64>(a, st);
         case 1: return dkv_reduce_typed<__half, 128>(a, st);
         case 2: return dkv_reduce_typed<__nv_bfloat16, 64>(a, st);
@@ -743,13 +745,15 @@ cudaError_t launch_dkv_reduce(int dtype, const BwdArgs &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
-bool uses_tc_bwd_fused(int dtype, int D_) { return (dtype == 0 || dtype == 1) && (D_ == 128 || D_ == 64); }
+bool uses_tc_bwd_fused(int dtype, int D_) {
+    return (dtype == 0 || dtype == 1) && (D_ == 32 || D_ == 64 || D_ == 96 || D_ == 128);
+}
 
 cudaError_t launch_tc_bwd_fused(int dtype, const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st) {
     // callers route problems without query rows to the two-kernel backward
     if (!a.dq_acc || (a.g.thd ? a.g.Tq : a.g.Sq) <= 0) return cudaErrorInvalidValue;
-    if (a.g.D == 64) return launch_tc_bwd_fused64(dtype, a, max_lkv, q_rows, st);
-    if (a.g.D != D) return cudaErrorInvalidValue;
+    if (tc_dim(a.g.D) == 64) return launch_tc_bwd_fused64(dtype, a, max_lkv, q_rows, st);
+    if (tc_dim(a.g.D) != D) return cudaErrorInvalidValue;
     switch (dtype) {
         case 0: return launch_typed<__half>(a, max_lkv, q_rows, st);
         case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, q_rows, st);

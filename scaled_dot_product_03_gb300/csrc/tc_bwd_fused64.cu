@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const MutView &ov = half == 0 ? a.dk : a.dv;
             T *dstp = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss + (int64_t)hk * ov.sh;
             store_row32<T>(dstp, *reinterpret_cast<uint32_t(*)[32]>(&v[0]), mul);
-            store_row32<T>(dstp + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]), mul);
+            if (g.D > 32) store_row32<T>(dstp + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]), mul);
         }
     } else if (warp >= kDrainWarp0) {
         // ------------------------------------- dQ drain (thread = query row)
@@ -473,8 +473,9 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
     const int dt = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
     const Geometry &g = a.g;
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
-    uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
-    uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
+    // inner extent: the real head dim (columns past it load as zeros)
+    uint64_t dq[4] = {(uint64_t)g.D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
+    uint64_t dk[4] = {(uint64_t)g.D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
     auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
         tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
@@ -519,7 +520,7 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
 }  // namespace
 
 cudaError_t launch_tc_bwd_fused64(int dtype, const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t st) {
-    if (a.g.D != D || !a.dq_acc) return cudaErrorInvalidValue;
+    if (tc_dim(a.g.D) != D || !a.dq_acc) return cudaErrorInvalidValue;
     switch (dtype) {
         case 0: return launch_typed<__half>(a, max_lkv, q_rows, st);
         case 1: return launch_typed<__nv_bfloat16>(a, max_lkv, q_rows, st);

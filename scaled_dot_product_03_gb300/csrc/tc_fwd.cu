@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = 0u;
                 }
-                if (valid) {
+                if (valid && cc * 32 < g.D) {
                     uint4 pk[4];
                     uint32_t *pw = reinterpret_cast<uint32_t *>(pk);
 #pragma unroll
@@ -445,8 +445,9 @@ cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t
     CUtensorMap tq, tk, tv, to;
     // dims (d, rows, heads, batch); THD: rows = all tokens, one batch
     const uint64_t nb = g.thd ? 1 : (uint64_t)g.B;
-    uint64_t dq[4] = {(uint64_t)D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
-    uint64_t dk[4] = {(uint64_t)D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
+    // inner extent: the real head dim (columns past it load as zeros)
+    uint64_t dq[4] = {(uint64_t)g.D, (uint64_t)g.Sq, (uint64_t)g.Hq, nb};
+    uint64_t dk[4] = {(uint64_t)g.D, (uint64_t)g.Skv, (uint64_t)g.Hkv, nb};
     auto strides = [&](const auto &v, const uint64_t dims[4], uint64_t out[3]) {
         tmap_strides(v.ss, v.sh, g.thd ? 0 : v.sb, dims, out);
     };
@@ -477,10 +478,12 @@ cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t
 
 }  // namespace
 
-bool uses_tc_fwd(int dtype, int D) { return (dtype == 0 || dtype == 1) && (D == 64 || D == 128); }
+bool uses_tc_fwd(int dtype, int D) {
+    return (dtype == 0 || dtype == 1) && (D == 32 || D == 64 || D == 96 || D == 128);
+}
 
 cudaError_t launch_tc_fwd(int dtype, const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
-    switch (dtype * 2 + (a.g.D == 128)) {
+    switch (dtype * 2 + (tc_dim(a.g.D) == 128)) {
         case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, st);
         case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, st);
         case 2: return launch_typed<__nv_bfloat16, 64>(a, max_lq, max_lkv, st);

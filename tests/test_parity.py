@@ -488,24 +488,55 @@ def test_cross_attention_few_queries_many_keys():
 
 # -------------------------------------------------------- other head dims
 
-@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype,det", [(torch.float16, False), (torch.bfloat16, False),
+                                       (torch.bfloat16, True), (torch.float32, False)])
 @pytest.mark.parametrize("D", [32, 96])
 @pytest.mark.parametrize("case", [
     dict(B=2, Sq=150, Skv=150, Hq=4, Hkv=2, window=(-1, 0)),
     dict(B=1, Sq=70, Skv=201, Hq=2, Hkv=1, window=(-1, -1)),
     dict(B=1, Sq=260, Skv=260, Hq=2, Hkv=2, window=(17, 3)),
+    dict(B=2, Sq=700, Skv=700, Hq=8, Hkv=8, window=(-1, 0)),
 ])
-def test_head_dims_32_and_96(dtype, D, case):
-    """Head dims outside the tensor-core kernels run on the FFMA kernels for
-    every element type (forward, backward, merge)."""
+def test_head_dims_32_and_96(dtype, D, det, case):
+    """Head dims 32 and 96: fp16 / bf16 on the 64- and 128-wide tensor-core
+    kernels with zero-padded columns (single pass and two-kernel backward),
+    fp32 on the FFMA kernels."""
     prob = inputs.dense(case["B"], case["Sq"], case["Hq"], D, dtype=dtype, window=case["window"],
                         Hkv=case["Hkv"], Skv=case["Skv"], seed=D + case["Sq"])
     d = _dev(prob)
     o, lse = run_fwd(d)
-    dq, dk, dv = run_bwd(d, o, lse)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
     _sync_ok()
     check_fwd(prob, o, lse)
     check_bwd(prob, dq, dk, dv)
+
+
+@pytest.mark.parametrize("D,det", [(32, False), (96, False), (96, True)])
+def test_head_dims_32_96_thd_padded_and_split(D, det):
+    """Padded head dims with THD (row-by-row stores of partial tiles), padded
+    cu_seqlens and grouped heads on a small grid (query-head split)."""
+    lengths = [300, 1, 517, 64, 0, 129]
+    prob = inputs.varlen(lengths=lengths, Hq=4, Hkv=1, D=D, dtype=torch.bfloat16, seed=D, dout_seed=D + 1)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse, deterministic=det)
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    check_bwd(prob, dq, dk, dv)
+
+
+@pytest.mark.parametrize("D", [32, 96])
+def test_head_dims_32_96_strided_views_equal_contiguous(D):
+    """A packed sb(h+2h_g)d buffer split into q, k, v views (the page-1
+    layout) at the padded head dims: the same results as contiguous copies."""
+    prob = inputs.page1(scale=0.1, seqlen=384, q_heads=4, kv_heads=2, head_dim=D, dout_seed=9)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    qc, kc, vc = (t.contiguous() for t in (d.q, d.k, d.v))
+    oc, lsec = gb.attn_fwd(qc, kc, vc, **kw(d))
+    _sync_ok()
+    assert torch.equal(o, oc) and torch.equal(lse, lsec)
+    check_fwd(prob, o, lse)
 
 
 # ------------------------------------------------------ randomized shapes
@@ -515,7 +546,7 @@ def _random_cases(n, seed=2024):
     cases = []
     for k in range(n):
         dtype = [torch.float16, torch.bfloat16][k % 2]
-        D = [64, 128][(k // 2) % 2]
+        D = [64, 128, 32, 96][(k // 2) % 4]
         Hkv = int(rng.choice([1, 2, 4]))
         Hq = Hkv * int(rng.choice([1, 2, 3]))
         window = [(-1, 0), (-1, -1), (int(rng.integers(0, 200)), 0),
@@ -534,7 +565,7 @@ def _random_cases(n, seed=2024):
     return cases
 
 
-@pytest.mark.parametrize("layout,args,det", _random_cases(24))
+@pytest.mark.parametrize("layout,args,det", _random_cases(32))
 def test_randomized_configs(layout, args, det):
     """Seeded random shapes across dtypes, head dims, layouts, grouped heads,
     windows and both backward forms, against the oracle."""
