@@ -348,6 +348,7 @@ def run_ours(args):
     if rank == 0 and not args.no_aux:
         aux["causal_fwd_bwd_sweep"] = sweep_lines(gb, inputs, dev, peaks["bf16_tflops"])
         aux.update(workload_lines(gb, inputs, dev, peaks["bf16_tflops"]))
+        aux.update(head_dim_and_mqa_lines(gb, inputs, dev, peaks["bf16_tflops"]))
     cpu = cpu_baseline(args) if rank == 0 and ws == 1 and not args.no_cpu else None
 
     if rank != 0:
@@ -528,6 +529,84 @@ def workload_lines(gb, inputs, dev, peak):
     return out
 
 
+def kernel_breakdown(gb, step, n=5):
+    """Mean live duration (ms) of each kernel kind over n profiled calls of
+    step(), from the library's per-launch timing hook."""
+    import torch
+    step()
+    torch.cuda.synchronize()
+    gb.profile_begin(64 * n)
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    per = {}
+    for name, ms in gb.profile_read(64 * n):
+        per.setdefault(name, []).append(ms)
+    return {k: round(sum(v) / n, 4) for k, v in per.items()}
+
+
+def head_dim_and_mqa_lines(gb, inputs, dev, peak):
+    """fwd / fwd+bwd TFLOP/s of: the page-1 workload (fp16, 16 query heads
+    over one KV head, packed strided views, S=2048) and causal bf16
+    multi-query attention against multi-head at equal flops (B2 S4096 H16
+    D128); head dims 32, 96 (padded tensor-core kernels) and 256 (forward
+    only) on causal bf16 B4 S4096 H16; the D=64 workload with its per-kernel
+    breakdown."""
+    import torch
+    out = {}
+
+    def measure(name, d, window, bwd=True, breakdown=False):
+        o, lse = gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=window)
+        fwd = lambda: gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=window, out=o, lse=lse)
+        lens = [d.Sq] * d.B
+        nvis = sum(n_visible(L, window) for L in lens) * d.Hq
+        f_fwd, f_bwd = 4.0 * d.D * nvis, 10.0 * d.D * nvis
+        ms_f = _time_steps(fwd, 20)
+        line = {"workload": name, "fwd_ms": round(ms_f, 4),
+                "fwd_TFLOP/s": round(f_fwd / (ms_f * 1e-3) / 1e12, 1),
+                "fwd_pct_of_peak": round(100 * f_fwd / (ms_f * 1e-3) / 1e12 / peak, 2)}
+        step = fwd
+        if bwd:
+            dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+            work = torch.empty(max(1, gb.attn_bwd_workspace_size(d.q, d.k, scale=d.scale, window=window)),
+                               dtype=torch.uint8, device=dev)
+
+            def step():
+                fwd()
+                gb.attn_bwd(d.dout, d.q, d.k, d.v, o, lse, scale=d.scale, window=window, dq=dq, dk=dk,
+                            dv=dv, workspace=work)
+            ms = _time_steps(step, 20)
+            tf = (f_fwd + f_bwd) / (ms * 1e-3) / 1e12
+            line.update({"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "pct_of_peak": round(100 * tf / peak, 2)})
+        if breakdown:
+            line["kernels_ms"] = kernel_breakdown(gb, step)
+        return line
+
+    d = inputs.page1(scale=0.1, dout_seed=5).to(dev)
+    assert d.q.stride() == (1152, 1152, 64, 1)
+    out["page1_mqa_fp16_strided"] = measure(
+        "fp16 causal S=2048, 16 query heads over 1 KV head, D=64, packed sb(h+2h_g)d views", d, (-1, 0),
+        breakdown=True)
+    del d
+    for hkv in (1, 16):
+        d = inputs.dense(2, 4096, 16, 128, Hkv=hkv, seed=3, dout_seed=4).to(dev)
+        out["causal_B2_S4096_H16_D128_Hkv%d" % hkv] = measure(
+            "bf16 causal B=2 S=4096, 16 query heads over %d KV heads, D=128" % hkv, d, (-1, 0),
+            breakdown=(hkv == 1))
+        del d
+    for D in (32, 96, 256):
+        d = inputs.dense(4, 4096, 16, D, seed=3, dout_seed=4 if D != 256 else None).to(dev)
+        out["causal_B4_S4096_H16_D%d" % D] = measure(
+            "bf16 causal B=4 S=4096 H=16 D=%d%s" % (D, " (forward only)" if D == 256 else
+                                                    " (on the %d-wide kernels)" % (64 if D == 32 else 128)),
+            d, (-1, 0), bwd=D != 256)
+        del d
+    d = inputs.dense(8, 1024, 16, 64, seed=3, dout_seed=4).to(dev)
+    out["causal_B8_S1024_H16_D64"] = measure("bf16 causal B=8 S=1024 H=16 D=64", d, (-1, 0), breakdown=True)
+    del d
+    return out
+
+
 def aux_lines(gb, inputs, dev, peaks):
     """LSE merge (HBM-bound) and fp32 forward+backward, timed on their own."""
     import torch
@@ -608,9 +687,20 @@ def aux_lines(gb, inputs, dev, peaks):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / n
     f_fwd, f_bwd, _ = flops(1, 512, 4, 64, (-1, -1))
+    # FFMA peak derived from the unit counts: SMs x 128 fp32 lanes x 2 flops
+    # x the maximum SM clock of MEASURED_PEAKS.json
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ffma_peak = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    tf32 = (f_fwd + f_bwd) / (ms * 1e-3) / 1e12
     out["fp32_page3"] = {"workload": "fp32 fwd+bwd B=1 S=512 H=4 D=64 non-causal",
-                         "ms": round(ms, 4),
-                         "TFLOP/s": round((f_fwd + f_bwd) / (ms * 1e-3) / 1e12, 3)}
+                         "ms": round(ms, 4), "TFLOP/s": round(tf32, 3),
+                         "bound": "alu", "ffma_peak_tflops": round(ffma_peak, 1),
+                         "ffma_peak_source": "derived: %d SMs x 128 lanes x 2 flops x max SM clock" % sms,
+                         "frac": round(tf32 / ffma_peak, 4),
+                         "kernels_ms": kernel_breakdown(gb, lambda: gb.attn_bwd(
+                             prob.dout, prob.q, prob.k, prob.v, *gb.attn_fwd(prob.q, prob.k, prob.v,
+                                                                             scale=prob.scale),
+                             scale=prob.scale))}
     return out
 
 

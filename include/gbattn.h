@@ -119,7 +119,8 @@ typedef struct {
     int Hq, Hkv;         /* query heads, key/value heads (Hq % Hkv == 0) */
     int D;               /* head dimension: 32, 64, 96 or 128 (tensor cores for
                             fp16 / bf16, 32 and 96 on the 64- and 128-wide
-                            kernels with zero padding; FFMA kernels for fp32) */
+                            kernels with zero padding; FFMA kernels for fp32),
+                            or 256 (fp16 / bf16 forward only) */
     const int32_t *cu_seqlens_q;  /* THD only: device, B + 1 non-decreasing */
     const int32_t *cu_seqlens_kv; /* offsets starting at 0 (NULL for DENSE4D) */
     int max_seqlen_q;    /* THD only: upper bound of the sequence lengths;

@@ -78,8 +78,8 @@ attn_status check_params(const attn_params *p) {
         return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d Sq=%d Skv=%d)", p->B, p->Sq, p->Skv);
     if (p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0)
         return fail(ATTN_ERR_INVALID_ARG, "Hq=%d must be a positive multiple of Hkv=%d", p->Hq, p->Hkv);
-    if (p->D != 32 && p->D != 64 && p->D != 96 && p->D != 128)
-        return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (32, 64, 96 or 128)", p->D);
+    if (p->D != 32 && p->D != 64 && p->D != 96 && p->D != 128 && p->D != 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (32, 64, 96, 128; 256 forward only)", p->D);
     if (p->deterministic != 0 && p->deterministic != 1)
         return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
     if (p->window_left < -1 || p->window_right < -1)
@@ -337,6 +337,8 @@ attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     t_error.clear();
     attn_status st = check_params(p);
     if (st != ATTN_OK) return st;
+    if (p->D == 256 && p->dtype == ATTN_F32)
+        return fail(ATTN_ERR_UNSUPPORTED, "head dim 256 runs on the fp16 / bf16 tensor-core forward only");
     if (p->B == 0 || max_lq(p) == 0) return ATTN_OK;  // no query row: nothing to write
     const int rq = p->Sq, rkv = p->Skv;
     if ((st = check_tensor(p, q, "q", rq, p->Hq)) || (st = check_tensor(p, k, "k", rkv, p->Hkv)) ||
@@ -362,7 +364,7 @@ attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
 }
 
 size_t attn_bwd_workspace_size(const attn_params *p) {
-    if (check_params(p) != ATTN_OK) return 0;
+    if (check_params(p) != ATTN_OK || p->D == 256) return 0;
     return ws_layout(p).total;
 }
 
@@ -377,6 +379,8 @@ attn_status bwd_impl(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     t_error.clear();
     attn_status st = check_params(p);
     if (st != ATTN_OK) return st;
+    if (p->D == 256)  // 256-column dK and dV accumulators do not fit the tensor memory
+        return fail(ATTN_ERR_UNSUPPORTED, "head dim 256: forward only");
     // Nothing to write when there is neither a query row (dq) nor a key row (dk, dv).
     if (p->B == 0 || (max_lq(p) == 0 && max_lkv(p) == 0)) return ATTN_OK;
     const int rq = p->Sq, rkv = p->Skv;

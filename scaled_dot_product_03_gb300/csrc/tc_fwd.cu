@@ -1,4 +1,4 @@
-// tc_fwd.cu -- tcgen05 forward attention for fp16 / bf16 (head dim 64, 128).
+// tc_fwd.cu -- tcgen05 forward attention for fp16 / bf16 (head dims 32 to 256).
 //
 // One CTA owns two 128-row query tiles of one (batch, query head) and walks
 // the key/value blocks of 128 rows that any of its rows can see (causal and
@@ -17,10 +17,12 @@
 // Warp roles (320 threads): warps 0-3 softmax + epilogue of tile 0, warps 4-7
 // the same for tile 1, warp 8 issues TMA loads, warp 9 allocates TMEM and
 // issues the MMAs.  Tiles are handed between roles with mbarriers; every wait
-// is bounded by the watchdog.
+// is bounded by the watchdog.  At head dim 256 a CTA owns one query tile
+// (192 threads: warps 0-3 softmax, 4 loads, 5 MMAs), since TMEM holds the
+// S and O of one tile only.
 //
 // TMEM columns (512 allocated): S/P of tile 0 at 0, of tile 1 at 128; O of
-// tile 0 at 256, of tile 1 at 256 + D.
+// tile 0 at 256, of tile 1 at 256 + D (one tile: S at 0, O at 128).
 #include <type_traits>
 
 #include "ptx.cuh"
@@ -35,17 +37,21 @@ using namespace ptx;
 
 constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per block
-constexpr int NQ = 2;            // query tiles per CTA
-constexpr int kThreads = 320;
-constexpr int kProdWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMaxNQ = 2;        // query tiles per CTA (one at D = 256)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct FwdCfg {
+    // Two query tiles per CTA ping-pong on the tensor pipe; at D = 256 the
+    // TMEM holds S (128 columns) and O (256) of one tile only, and shared
+    // memory one 64 KB K and V stage.
+    static constexpr int NQ = D == 256 ? 1 : 2;
+    static constexpr int kProdWarp = 4 * NQ;               // after the softmax warps
+    static constexpr int kMmaWarp = 4 * NQ + 1;
+    static constexpr int kThreads = 32 * (4 * NQ + 2);
     static constexpr int kChunks = D / 64;                 // 64-element swizzle atoms per row
     static constexpr int kTileBytes = BM * D * 2;          // one 128 x D tile
-    static constexpr int kStages = D == 128 ? 2 : 3;
+    static constexpr int kStages = D == 256 ? 1 : D == 128 ? 2 : 3;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + NQ * kTileBytes;
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
@@ -56,7 +62,7 @@ struct FwdCfg {
 struct Bars {
     uint64_t q_full;
     uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
-    uint64_t s_full[NQ], p_full[NQ], pv_done[NQ];
+    uint64_t s_full[kMaxNQ], p_full[kMaxNQ], pv_done[kMaxNQ];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -85,12 +91,15 @@ struct TileRange {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, FwdArgs a,
                   int n_mtiles) {
     using C = FwdCfg<D>;
     constexpr int KS = C::kStages;
+    constexpr int NQ = C::NQ;
+    constexpr int kProdWarp = C::kProdWarp;
+    constexpr int kMmaWarp = C::kMmaWarp;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < BN / 16; ++kk)
-                                mma_ts(tmem + 2 * BN + i * D, tmem + i * BN + kk * 8, desc_add(dv, kk * 16 * 128),
+                                mma_ts(tmem + NQ * BN + i * D, tmem + i * BN + kk * 8, desc_add(dv, kk * 16 * 128),
                                        idPV, kk > 0 ? 1u : acc0);
                             mma_commit(&bar.pv_done[i]);
                         }
@@ -273,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = tr[i].row0 + r;  // row within the sequence
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + i * BN + lane_off;
-        const uint32_t tO = tmem + 2 * BN + i * D + lane_off;
+        const uint32_t tO = tmem + NQ * BN + i * D + lane_off;
         const int n_i = tr[i].bhi - tr[i].blo;
         const float c2 = g.scale_log2;
         float m = -INFINITY, l = 0.f;
@@ -466,12 +475,13 @@ cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
         cudaSuccess)
         return e;
+    constexpr int NQ = FwdCfg<D>::NQ;
     const int n_mtiles = (max_lq + BM * NQ - 1) / (BM * NQ);
     const int64_t grid = (int64_t)n_mtiles * g.Hq * g.B;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
     prof_before(st, kProfFwd);
-    kern<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, to, a, n_mtiles);
+    kern<<<(unsigned)grid, FwdCfg<D>::kThreads, smem, st>>>(tq, tk, tv, to, a, n_mtiles);
     prof_after(st);
     return cudaGetLastError();
 }
@@ -479,10 +489,15 @@ cudaError_t launch_typed(const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t
 }  // namespace
 
 bool uses_tc_fwd(int dtype, int D) {
-    return (dtype == 0 || dtype == 1) && (D == 32 || D == 64 || D == 96 || D == 128);
+    return (dtype == 0 || dtype == 1) && (D == 32 || D == 64 || D == 96 || D == 128 || D == 256);
 }
 
 cudaError_t launch_tc_fwd(int dtype, const FwdArgs &a, int max_lq, int max_lkv, cudaStream_t st) {
+    if (a.g.D == 256) {
+        if (dtype == 0) return launch_typed<__half, 256>(a, max_lq, max_lkv, st);
+        if (dtype == 1) return launch_typed<__nv_bfloat16, 256>(a, max_lq, max_lkv, st);
+        return cudaErrorInvalidValue;
+    }
     switch (dtype * 2 + (tc_dim(a.g.D) == 128)) {
         case 0: return launch_typed<__half, 64>(a, max_lq, max_lkv, st);
         case 1: return launch_typed<__half, 128>(a, max_lq, max_lkv, st);

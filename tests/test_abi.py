@@ -253,3 +253,18 @@ def test_strides_beyond_tensor_map_reach_rejected(lib, which):
         p1 = _params(B=1)
         st = lib.attn_fwd(ctypes.byref(p1), bad, bad, bad, bad, 0, None)
         assert st == _lib.ATTN_ERR_INVALID_ARG  # only the NULL lse is left to reject
+
+
+def test_head_dim_256_is_a_16_bit_forward_only(lib):
+    """Head dim 256 runs on the fp16 / bf16 tensor-core forward; the backward
+    (whose 256-column dK and dV accumulators do not fit the tensor memory) and
+    fp32 are refused before anything is enqueued."""
+    p = _params(D=256)
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == 0
+    t = _t(strides=(32768 * 4, 1024, 256, 1))
+    st = lib.attn_bwd(ctypes.byref(p), t, t, t, t, t, 4096, t, t, t, 4096, 1 << 20, None)
+    assert st == _lib.ATTN_ERR_UNSUPPORTED and b"forward only" in lib.attn_last_error_string()
+    p32 = _params(D=256, dtype=_lib.ATTN_F32)
+    st = lib.attn_fwd(ctypes.byref(p32), t, t, t, t, 4096, None)
+    assert st == _lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd(ctypes.byref(_params(D=192)), t, t, t, t, 4096, None) == _lib.ATTN_ERR_UNSUPPORTED

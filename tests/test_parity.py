@@ -539,6 +539,36 @@ def test_head_dims_32_96_strided_views_equal_contiguous(D):
     check_fwd(prob, o, lse)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("case", [
+    dict(B=2, Sq=300, Skv=300, Hq=4, Hkv=2, window=(-1, 0)),
+    dict(B=1, Sq=70, Skv=201, Hq=2, Hkv=1, window=(-1, -1)),
+    dict(B=1, Sq=520, Skv=520, Hq=2, Hkv=2, window=(40, 3)),
+    dict(B=1, Sq=150, Skv=90, Hq=2, Hkv=1, window=(0, 0)),
+])
+def test_head_dim_256_forward(dtype, case):
+    """Head dim 256 (forward only): one query tile per CTA, S and O of the
+    tile in TMEM, N = 256 for O += P V."""
+    prob = inputs.dense(case["B"], case["Sq"], case["Hq"], 256, dtype=dtype, window=case["window"],
+                        Hkv=case["Hkv"], Skv=case["Skv"], seed=256 + case["Sq"], dout_seed=None)
+    o, lse = run_fwd(_dev(prob))
+    _sync_ok()
+    check_fwd(prob, o, lse)
+
+
+def test_head_dim_256_forward_thd_and_full_size_sampled():
+    """Head dim 256 with THD (row-by-row stores of partial tiles) and at a
+    long causal sequence, on sampled rows."""
+    prob = inputs.varlen(lengths=[300, 1, 517, 64, 0, 129], Hq=4, Hkv=2, D=256, seed=2, dout_seed=None)
+    o, lse = run_fwd(_dev(prob))
+    _sync_ok()
+    check_fwd(prob, o, lse)
+    prob = inputs.dense(1, 8192, 8, 256, seed=4, dout_seed=None)
+    o, lse = run_fwd(_dev(prob))
+    _sync_ok()
+    check_fwd(prob, o, lse, row_sel=sample_rows(prob, 48, seed=4))
+
+
 # ------------------------------------------------------ randomized shapes
 
 def _random_cases(n, seed=2024):
