@@ -769,6 +769,101 @@ def run_reference(args):
     }
 
 
+# Small workloads, one per kernel, for profiler captures (one kernel per
+# capture, a few launches): name -> (description, builder).  Each builder
+# returns a callable running the case once; the captured kernel is named in
+# the profile summaries.
+def _profile_cases():
+    import torch
+    import scaled_dot_product_03_gb300 as gb
+    from scaled_dot_product_03_gb300 import inputs
+    dev = torch.device("cuda", 0)
+
+    def fwd_bwd(prob, window=(-1, 0), det=False, extra=None):
+        d = prob.to(dev)
+        extra = extra or {}
+        o, lse = gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=window, **extra)
+        dq, dk, dv = torch.empty_like(d.q), torch.empty_like(d.k), torch.empty_like(d.v)
+        work = torch.empty(max(1, gb.attn_bwd_workspace_size(d.q, d.k, scale=d.scale, window=window,
+                                                             deterministic=det, **extra)),
+                           dtype=torch.uint8, device=dev)
+
+        def run():
+            gb.attn_fwd(d.q, d.k, d.v, scale=d.scale, window=window, out=o, lse=lse, **extra)
+            if d.dout is not None:
+                gb.attn_bwd(d.dout, d.q, d.k, d.v, o, lse, scale=d.scale, window=window, dq=dq, dk=dk, dv=dv,
+                            workspace=work, deterministic=det, **extra)
+        return run
+
+    def merge():
+        g = torch.Generator().manual_seed(5)
+        B, S, H, D = 4, 4096, 16, 128
+        o1, o2, do = (torch.randn(B, S, H, D, generator=g).bfloat16().to(dev) for _ in range(3))
+        l1, l2, dl = (torch.randn(B, H, S, generator=g).to(dev) for _ in range(3))
+        oo, lo = torch.empty_like(o1), torch.empty_like(l1)
+        gr = [torch.empty_like(o1), torch.empty_like(l1), torch.empty_like(o2), torch.empty_like(l2)]
+
+        def run():
+            gb.attn_merge_lse(o1, l1, o2, l2, out=oo, lse_out=lo)
+            gb.attn_merge_lse_bwd(o1, l1, o2, l2, do, dl, do1=gr[0], dlse1=gr[1], do2=gr[2], dlse2=gr[3])
+        return run
+
+    def partition():
+        from scaled_dot_product_03_gb300 import _lib
+        import ctypes
+        lens = [262144] * 64
+        pads = [0]
+        for L in lens:
+            pads.append(pads[-1] + L)
+        pad = torch.tensor(pads, dtype=torch.int32, device=dev)
+        out = torch.empty(pads[-1] // 4, dtype=torch.int32, device=dev)
+        lib = _lib.load()
+
+        def run():
+            _lib.check(lib.attn_thd_partitioned_indices(pad.data_ptr(), len(lens), pads[-1], 4, 1, out.data_ptr(),
+                                                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+        return run
+
+    return {
+        "causal_bf16_b2_s8192_h8_d128": ("tc_fwd<bf16,128>, single-pass backward, preprocess, dq convert",
+                                         lambda: fwd_bwd(inputs.dense(2, 8192, 8, 128, seed=3, dout_seed=4))),
+        "causal_bf16_b2_s8192_h8_d128_det": ("the two-kernel backward (tc_bwd_dkdv, tc_bwd_dq)",
+                                             lambda: fwd_bwd(inputs.dense(2, 8192, 8, 128, seed=3, dout_seed=4),
+                                                             det=True)),
+        "causal_bf16_b8_s1024_h16_d64": ("tc_fwd<bf16,64>, single-pass backward at D=64",
+                                         lambda: fwd_bwd(inputs.dense(8, 1024, 16, 64, seed=3, dout_seed=4))),
+        "causal_bf16_b2_s4096_h16_d128_mqa": ("query-head split and the dK/dV reduce (one KV head)",
+                                              lambda: fwd_bwd(inputs.dense(2, 4096, 16, 128, Hkv=1, seed=3,
+                                                                           dout_seed=4))),
+        "causal_bf16_b1_s8192_h8_d256": ("tc_fwd<bf16,256> (forward only)",
+                                         lambda: fwd_bwd(inputs.dense(1, 8192, 8, 256, seed=3, dout_seed=None))),
+        "fp32_causal_b4_s2048_h16_d64": ("FFMA forward, dq and dk/dv kernels",
+                                         lambda: fwd_bwd(inputs.dense(4, 2048, 16, 64, dtype=torch.float32, seed=3,
+                                                                      dout_seed=4))),
+        "merge_bf16_b4_s4096_h16_d128": ("LSE merge and its backward", merge),
+        "thd_partition_64x262144_cp4": ("THD context-parallel partition (rank 1 of 4)", partition),
+    }
+
+
+def run_profile_case(name, repeats):
+    """Runs one profiling workload `repeats` times (no timing, no output but
+    a line naming the case); for profiler captures of one kernel."""
+    import torch
+    from scaled_dot_product_03_gb300 import build as libbuild
+    import scaled_dot_product_03_gb300 as gb
+    libbuild.build()
+    cases = _profile_cases()
+    if name not in cases:
+        raise SystemExit("unknown profile case %r (known: %s)" % (name, ", ".join(sorted(cases))))
+    desc, make = cases[name]
+    run = make()
+    for _ in range(repeats):
+        run()
+    torch.cuda.synchronize()
+    gb.check_device_error()
+    print("profile case %s (%s): %d runs" % (name, desc, repeats))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -780,7 +875,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--shape", default=None,
                     help="B,S,H,D of the causal workload (default: the headline workload)")
+    ap.add_argument("--profile-case", default=None,
+                    help="run one small per-kernel workload for a profiler capture and exit")
+    ap.add_argument("--repeats", type=int, default=3, help="runs of --profile-case")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.repeats)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     line = run_reference(args) if args.impl == "reference" else run_ours(args)

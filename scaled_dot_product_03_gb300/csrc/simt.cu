@@ -6,11 +6,14 @@
 // here with plain fp32 fused multiply-adds and never reach a tensor core.
 // Every kernel also accepts fp16/bf16 inputs (converted to fp32 on load).
 //
-// Forward: one thread per query row, online softmax over key blocks staged
-// in shared memory (an exact rewrite of the two-pass softmax).
+// Forward: one lane per query row and the rows' keys split over the CTA's
+// warps, each with an online softmax over its key blocks (an exact rewrite of
+// the two-pass softmax), the warps' partial results combined at the end.
 // Backward: the row term delta_i = <dO_i, O_i> first, then one kernel for dq
-// (thread per query row) and one for dk/dv (four threads per key, summing
-// over the query heads of the group), each recomputing P from the saved LSE.
+// (lane per query row, keys split over warps) and one for dk/dv (four threads
+// per key, the query blocks of the group's heads split over thread groups),
+// each recomputing P from the saved LSE and summing partials in shared
+// memory.
 #include "launch.h"
 #include "prof.h"
 
@@ -18,6 +21,11 @@ namespace gbattn {
 namespace {
 
 constexpr int kThreads = 128;
+
+// Barrier among `n` threads (a multiple of 32) on named barrier `id` (1-15).
+__device__ __forceinline__ void ptx_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 template <typename T>
 __device__ __forceinline__ const T *row_ptr(const View &v, int b, int row, int h) {
@@ -29,34 +37,52 @@ __device__ __forceinline__ T *row_ptr(const MutView &v, int b, int row, int h) {
 }
 
 // ---------------------------------------------------------------------------
-// Forward.  grid (ceil(max Lq / 128), Hq, B), 128 threads; thread = query row.
-// smem: Q^T [D][129] (padded so row-per-thread reads are conflict-free),
-// K and V blocks [BN][D], all fp32.
+// Work split of the query-row kernels (forward and dq): a CTA takes kRows
+// query rows (lane = row) and kSplits warps; warp w walks key blocks
+// w, w + kSplits, ... of the rows' key range, staging each block of BN keys
+// in its own slice of shared memory, and the warps' partial results are
+// combined through shared memory at the end.  Splitting the keys over warps
+// (rather than one thread per row over all keys) puts kSplits times more
+// warps on short problems such as the page-3 workload.
+constexpr int kRows = 32;
+constexpr int kSplits = 8;
+constexpr int kSplitThreads = kRows * kSplits;
+constexpr int kBN = 16;  // keys per block and warp
+
+// Forward.  grid (ceil(max Lq / kRows), Hq, B), kSplitThreads threads.
+// smem: Q^T [D][kRows] (lane-consecutive reads), per warp a K and a V block
+// [kBN][D]; afterwards the partial (m, l, o) of every warp.  Each warp keeps
+// an online softmax over its blocks (an exact rewrite of the two-pass
+// softmax); the combination rescales the partials by exp2(m_w - max m).
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
-    constexpr int BM = kThreads, BN = (D > 64) ? 16 : 32, QP = BM + 1;
+__global__ void __launch_bounds__(kSplitThreads) simt_fwd_kernel(FwdArgs a) {
     extern __shared__ float smem[];
-    float *Qs = smem, *Ks = Qs + D * QP, *Vs = Ks + BN * D;
+    float *Qs = smem, *KV = Qs + D * kRows;
     const Geometry &g = a.g;
-    const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * BM, tid = threadIdx.x;
+    const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * kRows, tid = threadIdx.x;
+    const int warp = tid / 32, lane = tid % 32;
     const SeqInfo s = seq_info(g, b);
-    if (blockIdx.x == gridDim.x - 1 && tid == 0) report_uncovered(a.err, g, s.Lq, gridDim.x * BM, kErrSeqlenQ);
+    if (blockIdx.x == gridDim.x - 1 && tid == 0) report_uncovered(a.err, g, s.Lq, gridDim.x * kRows, kErrSeqlenQ);
     if (m0 >= s.Lq) return;
-    const int hk = h / g.G, i = m0 + tid;
-    for (int e = tid; e < BM * D; e += kThreads) {
+    const int hk = h / g.G, i = m0 + lane;
+    for (int e = tid; e < kRows * D; e += kSplitThreads) {
         const int r = e / D, d = e % D;
         float x = 0.f;
         if (m0 + r < s.Lq) x = to_f32(row_ptr<T>(a.q, b, s.q0 + m0 + r, h)[d]);
-        Qs[d * QP + r] = x;
+        Qs[d * kRows + r] = x;
     }
     int jlo, jhi;
-    key_range(m0, min(m0 + BM, s.Lq), s.Lkv, g.wl, g.wr, jlo, jhi);
+    key_range(m0, min(m0 + kRows, s.Lq), s.Lkv, g.wl, g.wr, jlo, jhi);
+    const int nblk = (jhi - jlo + kBN - 1) / kBN;
+    __syncthreads();
+    float *Ks = KV + warp * 2 * kBN * D, *Vs = Ks + kBN * D;
     float m = -INFINITY, l = 0.f, o[D];
 #pragma unroll
     for (int d = 0; d < D; ++d) o[d] = 0.f;
-    for (int j0 = jlo; j0 < jhi; j0 += BN) {
-        __syncthreads();
-        for (int e = tid; e < BN * D; e += kThreads) {
+    for (int bi = warp; bi < nblk; bi += kSplits) {
+        const int j0 = jlo + bi * kBN;
+        __syncwarp();
+        for (int e = lane; e < kBN * D; e += 32) {
             const int r = e / D, d = e % D, j = j0 + r;
             float kx = 0.f, vx = 0.f;
             if (j < jhi) {
@@ -66,19 +92,19 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
             Ks[e] = kx;
             Vs[e] = vx;
         }
-        __syncthreads();
-        float sc[BN];
+        __syncwarp();
+        float sc[kBN];
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) sc[jj] = 0.f;
+        for (int jj = 0; jj < kBN; ++jj) sc[jj] = 0.f;
 #pragma unroll 4
         for (int d = 0; d < D; ++d) {
-            const float qd = Qs[d * QP + tid];
+            const float qd = Qs[d * kRows + lane];
 #pragma unroll
-            for (int jj = 0; jj < BN; ++jj) sc[jj] = fmaf(qd, Ks[jj * D + d], sc[jj]);
+            for (int jj = 0; jj < kBN; ++jj) sc[jj] = fmaf(qd, Ks[jj * D + d], sc[jj]);
         }
         float mx = m;
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) {
+        for (int jj = 0; jj < kBN; ++jj) {
             const int j = j0 + jj;
             const bool vis = i < s.Lq && j < jhi && visible(i, j, s.Lkv, g.wl, g.wr);
             if (!vis) sc[jj] = -INFINITY;
@@ -90,24 +116,50 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(FwdArgs a) {
 #pragma unroll
         for (int d = 0; d < D; ++d) o[d] *= alpha;
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) {
+        for (int jj = 0; jj < kBN; ++jj) {
             const float p = sc[jj] == -INFINITY ? 0.f : exp2f(fmaf(sc[jj], g.scale_log2, -mx));
             l += p;
             sc[jj] = p;
         }
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) {
+        for (int jj = 0; jj < kBN; ++jj) {
 #pragma unroll
             for (int d = 0; d < D; ++d) o[d] = fmaf(sc[jj], Vs[jj * D + d], o[d]);
         }
         m = mx;
     }
-    if (i < s.Lq) {
-        T *orow = row_ptr<T>(a.o, b, s.q0 + i, h);
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+    // partials of every warp: o^T [kSplits][D][kRows], m and l [kSplits][kRows]
+    __syncthreads();
+    float *Op = KV, *Mp = Op + kSplits * D * kRows, *Lp = Mp + kSplits * kRows;
 #pragma unroll
-        for (int d = 0; d < D; ++d) orow[d] = from_f32<T>(o[d] * inv);
-        a.lse[lse_index(g, s, b, h, i)] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    for (int d = 0; d < D; ++d) Op[(warp * D + d) * kRows + lane] = o[d];
+    Mp[warp * kRows + lane] = m;
+    Lp[warp * kRows + lane] = l;
+    __syncthreads();
+    // thread (warp, lane): row lane, head dims [warp D / kSplits, (warp + 1) D / kSplits)
+    float mt = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kSplits; ++w) mt = fmaxf(mt, Mp[w * kRows + lane]);
+    float wt[kSplits], lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSplits; ++w) {
+        const float mw = Mp[w * kRows + lane];
+        wt[w] = mw == -INFINITY ? 0.f : exp2f(mw - mt);
+        lt = fmaf(Lp[w * kRows + lane], wt[w], lt);
+    }
+    if (i < s.Lq) {
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        T *orow = row_ptr<T>(a.o, b, s.q0 + i, h);
+        constexpr int DS = D / kSplits;
+#pragma unroll 8
+        for (int e = 0; e < DS; ++e) {
+            const int d = warp * DS + e;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kSplits; ++w) acc = fmaf(Op[(w * D + d) * kRows + lane], wt[w], acc);
+            orow[d] = from_f32<T>(acc * inv);
+        }
+        if (warp == 0) a.lse[lse_index(g, s, b, h, i)] = lt > 0.f ? (mt + log2f(lt)) * kLn2 : -INFINITY;
     }
 }
 
@@ -247,27 +299,30 @@ __global__ void __launch_bounds__(256) bwd_preprocess16_kernel(BwdArgs a, int ro
 }
 
 // ---------------------------------------------------------------------------
-// Backward dq: thread = query row; K, V blocks in shared memory.
+// Backward dq, with the work split of the forward: grid (ceil(max Lq /
+// kRows), Hq, B), kSplitThreads threads; lane = query row, warps split the
+// keys; smem Q^T and dO^T [D][kRows], per warp a K and a V block, then the
+// warps' partial dq [kSplits][D][kRows], summed at the end.
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(BwdArgs a) {
-    constexpr int BM = kThreads, BN = 16, QP = BM + 1;
+__global__ void __launch_bounds__(kSplitThreads) simt_bwd_dq_kernel(BwdArgs a) {
     extern __shared__ float smem[];
-    float *Qs = smem, *Os = Qs + D * QP, *Ks = Os + D * QP, *Vs = Ks + BN * D;
+    float *Qs = smem, *Os = Qs + D * kRows, *KV = Os + D * kRows;
     const Geometry &g = a.g;
-    const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * BM, tid = threadIdx.x;
+    const int b = blockIdx.z, h = blockIdx.y, m0 = blockIdx.x * kRows, tid = threadIdx.x;
+    const int warp = tid / 32, lane = tid % 32;
     const SeqInfo s = seq_info(g, b);
-    if (blockIdx.x == gridDim.x - 1 && tid == 0) report_uncovered(a.err, g, s.Lq, gridDim.x * BM, kErrSeqlenQ);
+    if (blockIdx.x == gridDim.x - 1 && tid == 0) report_uncovered(a.err, g, s.Lq, gridDim.x * kRows, kErrSeqlenQ);
     if (m0 >= s.Lq) return;
-    const int hk = h / g.G, i = m0 + tid;
-    for (int e = tid; e < BM * D; e += kThreads) {
+    const int hk = h / g.G, i = m0 + lane;
+    for (int e = tid; e < kRows * D; e += kSplitThreads) {
         const int r = e / D, d = e % D;
         float x = 0.f, y = 0.f;
         if (m0 + r < s.Lq) {
             x = to_f32(row_ptr<T>(a.q, b, s.q0 + m0 + r, h)[d]);
             y = to_f32(row_ptr<T>(a.dout, b, s.q0 + m0 + r, h)[d]);
         }
-        Qs[d * QP + r] = x;
-        Os[d * QP + r] = y;  // dO^T
+        Qs[d * kRows + r] = x;
+        Os[d * kRows + r] = y;  // dO^T
     }
     float lse_l2 = 0.f, delta = 0.f;
     if (i < s.Lq) {
@@ -276,13 +331,17 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(BwdArgs a) {
         delta = a.delta[li];
     }
     int jlo, jhi;
-    key_range(m0, min(m0 + BM, s.Lq), s.Lkv, g.wl, g.wr, jlo, jhi);
+    key_range(m0, min(m0 + kRows, s.Lq), s.Lkv, g.wl, g.wr, jlo, jhi);
+    const int nblk = (jhi - jlo + kBN - 1) / kBN;
+    __syncthreads();
+    float *Ks = KV + warp * 2 * kBN * D, *Vs = Ks + kBN * D;
     float dq[D];
 #pragma unroll
     for (int d = 0; d < D; ++d) dq[d] = 0.f;
-    for (int j0 = jlo; j0 < jhi; j0 += BN) {
-        __syncthreads();
-        for (int e = tid; e < BN * D; e += kThreads) {
+    for (int bi = warp; bi < nblk; bi += kSplits) {
+        const int j0 = jlo + bi * kBN;
+        __syncwarp();
+        for (int e = lane; e < kBN * D; e += 32) {
             const int r = e / D, d = e % D, j = j0 + r;
             float kx = 0.f, vx = 0.f;
             if (j < jhi) {
@@ -292,21 +351,21 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(BwdArgs a) {
             Ks[e] = kx;
             Vs[e] = vx;
         }
-        __syncthreads();
-        float sc[BN], dp[BN];
+        __syncwarp();
+        float sc[kBN], dp[kBN];
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) sc[jj] = dp[jj] = 0.f;
+        for (int jj = 0; jj < kBN; ++jj) sc[jj] = dp[jj] = 0.f;
 #pragma unroll 4
         for (int d = 0; d < D; ++d) {
-            const float qd = Qs[d * QP + tid], od = Os[d * QP + tid];
+            const float qd = Qs[d * kRows + lane], od = Os[d * kRows + lane];
 #pragma unroll
-            for (int jj = 0; jj < BN; ++jj) {
+            for (int jj = 0; jj < kBN; ++jj) {
                 sc[jj] = fmaf(qd, Ks[jj * D + d], sc[jj]);
                 dp[jj] = fmaf(od, Vs[jj * D + d], dp[jj]);
             }
         }
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) {
+        for (int jj = 0; jj < kBN; ++jj) {
             const int j = j0 + jj;
             float ds = 0.f;
             if (i < s.Lq && j < jhi && visible(i, j, s.Lkv, g.wl, g.wr)) {
@@ -316,34 +375,55 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(BwdArgs a) {
             sc[jj] = ds;
         }
 #pragma unroll
-        for (int jj = 0; jj < BN; ++jj) {
+        for (int jj = 0; jj < kBN; ++jj) {
 #pragma unroll
             for (int d = 0; d < D; ++d) dq[d] = fmaf(sc[jj], Ks[jj * D + d], dq[d]);
         }
     }
+    __syncthreads();
+    float *Qp = KV;  // [kSplits][D][kRows]
+#pragma unroll
+    for (int d = 0; d < D; ++d) Qp[(warp * D + d) * kRows + lane] = dq[d];
+    __syncthreads();
     if (i < s.Lq) {
         T *row = row_ptr<T>(a.dq, b, s.q0 + i, h);
+        constexpr int DS = D / kSplits;
+#pragma unroll 8
+        for (int e = 0; e < DS; ++e) {
+            const int d = warp * DS + e;
+            float acc = 0.f;
 #pragma unroll
-        for (int d = 0; d < D; ++d) row[d] = from_f32<T>(dq[d] * g.scale);
+            for (int w = 0; w < kSplits; ++w) acc += Qp[(w * D + d) * kRows + lane];
+            row[d] = from_f32<T>(acc * g.scale);
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
-// Backward dk, dv: four threads per key (thread part p owns d = p, p+4, ...),
-// 32 keys per CTA; loops over the query heads of the group and over query
-// blocks of 32 rows staged in shared memory.
+// Backward dk, dv: four threads per key (thread part p owns d = p, p + 4,
+// ...), kKeys keys per CTA, and kGroups groups of such threads that split
+// the (query head, query block) pairs of the keys' group between them, each
+// staging its own query blocks of kQB rows; the groups' partial dk and dv
+// are summed through shared memory at the end.
+constexpr int kKeys = 16;
+constexpr int kGroups = 4;
+constexpr int kQB = 16;
+constexpr int kKvThreads = kKeys * 4 * kGroups;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(BwdArgs a) {
-    constexpr int BN = kThreads / 4, BM = 32, DP = D / 4;
+__global__ void __launch_bounds__(kKvThreads) simt_bwd_dkdv_kernel(BwdArgs a) {
+    constexpr int DP = D / 4;
+    constexpr int kGroupFloats = 2 * kQB * D + 2 * kQB;  // Q, dO, lse, delta of one group
     extern __shared__ float smem[];
-    float *Qs = smem, *Os = Qs + BM * D, *Ls = Os + BM * D, *Ds = Ls + BM;
     const Geometry &g = a.g;
-    const int b = blockIdx.z, hk = blockIdx.y, n0 = blockIdx.x * BN, tid = threadIdx.x;
+    const int b = blockIdx.z, hk = blockIdx.y, n0 = blockIdx.x * kKeys, tid = threadIdx.x;
+    const int grp = tid / (kKeys * 4), gt = tid % (kKeys * 4);
+    float *Qs = smem + grp * kGroupFloats, *Os = Qs + kQB * D, *Ls = Os + kQB * D, *Ds = Ls + kQB;
     const SeqInfo s = seq_info(g, b);
     if (blockIdx.x == gridDim.x - 1 && tid == 0)
-        report_uncovered(a.err, g, s.Lkv, gridDim.x * BN, kErrSeqlenKv);
+        report_uncovered(a.err, g, s.Lkv, gridDim.x * kKeys, kErrSeqlenKv);
     if (n0 >= s.Lkv) return;
-    const int kt = tid / 4, part = tid % 4, j = n0 + kt;
+    const int kt = gt / 4, part = gt % 4, j = n0 + kt;
     float kr[DP], vr[DP], dk[DP], dv[DP];
 #pragma unroll
     for (int t = 0; t < DP; ++t) {
@@ -354,77 +434,105 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(BwdArgs a) {
         }
     }
     int ilo, ihi;
-    query_range(n0, min(n0 + BN, s.Lkv), s.Lq, g.wl, g.wr, ilo, ihi);
-    for (int h = hk * g.G; h < (hk + 1) * g.G; ++h) {
-        for (int i0 = ilo; i0 < ihi; i0 += BM) {
-            __syncthreads();
-            for (int e = tid; e < BM * D; e += kThreads) {
-                const int r = e / D, d = e % D, i = i0 + r;
-                float x = 0.f, y = 0.f;
-                if (i < ihi) {
-                    x = to_f32(row_ptr<T>(a.q, b, s.q0 + i, h)[d]);
-                    y = to_f32(row_ptr<T>(a.dout, b, s.q0 + i, h)[d]);
-                }
-                Qs[e] = x;
-                Os[e] = y;
+    query_range(n0, min(n0 + kKeys, s.Lkv), s.Lq, g.wl, g.wr, ilo, ihi);
+    const int nqb = (ihi - ilo + kQB - 1) / kQB;
+    const int n_pairs = nqb * g.G;
+    for (int t0 = grp; t0 < n_pairs; t0 += kGroups) {
+        const int h = hk * g.G + t0 / nqb, i0 = ilo + (t0 % nqb) * kQB;
+        ptx_bar_sync(1 + grp, kKeys * 4);  // the group's previous block is read
+        for (int e = gt; e < kQB * D; e += kKeys * 4) {
+            const int r = e / D, d = e % D, i = i0 + r;
+            float x = 0.f, y = 0.f;
+            if (i < ihi) {
+                x = to_f32(row_ptr<T>(a.q, b, s.q0 + i, h)[d]);
+                y = to_f32(row_ptr<T>(a.dout, b, s.q0 + i, h)[d]);
             }
-            for (int r = tid; r < BM; r += kThreads) {
-                const int i = i0 + r;
-                float lv = 0.f, dv_ = 0.f;
-                if (i < ihi) {
-                    const int64_t li = lse_index(g, s, b, h, i);
-                    lv = a.lse[li] * kLog2e;
-                    dv_ = a.delta[li];
-                }
-                Ls[r] = lv;
-                Ds[r] = dv_;
+            Qs[e] = x;
+            Os[e] = y;
+        }
+        for (int r = gt; r < kQB; r += kKeys * 4) {
+            const int i = i0 + r;
+            float lv = 0.f, dv_ = 0.f;
+            if (i < ihi) {
+                const int64_t li = lse_index(g, s, b, h, i);
+                lv = a.lse[li] * kLog2e;
+                dv_ = a.delta[li];
             }
-            __syncthreads();
-            for (int r = 0; r < BM; ++r) {
-                const int i = i0 + r;
-                float sp = 0.f, dpp = 0.f;
+            Ls[r] = lv;
+            Ds[r] = dv_;
+        }
+        ptx_bar_sync(1 + grp, kKeys * 4);
+        for (int r = 0; r < kQB; ++r) {
+            const int i = i0 + r;
+            float sp = 0.f, dpp = 0.f;
+#pragma unroll
+            for (int t = 0; t < DP; ++t) {
+                sp = fmaf(Qs[r * D + 4 * t + part], kr[t], sp);
+                dpp = fmaf(Os[r * D + 4 * t + part], vr[t], dpp);
+            }
+            sp += __shfl_xor_sync(0xffffffffu, sp, 1);
+            sp += __shfl_xor_sync(0xffffffffu, sp, 2);
+            dpp += __shfl_xor_sync(0xffffffffu, dpp, 1);
+            dpp += __shfl_xor_sync(0xffffffffu, dpp, 2);
+            if (i < ihi && visible(i, j, s.Lkv, g.wl, g.wr)) {
+                const float p = exp2f(fmaf(sp, g.scale_log2, -Ls[r]));
+                const float ds = p * (dpp - Ds[r]);
 #pragma unroll
                 for (int t = 0; t < DP; ++t) {
-                    sp = fmaf(Qs[r * D + 4 * t + part], kr[t], sp);
-                    dpp = fmaf(Os[r * D + 4 * t + part], vr[t], dpp);
-                }
-                sp += __shfl_xor_sync(0xffffffffu, sp, 1);
-                sp += __shfl_xor_sync(0xffffffffu, sp, 2);
-                dpp += __shfl_xor_sync(0xffffffffu, dpp, 1);
-                dpp += __shfl_xor_sync(0xffffffffu, dpp, 2);
-                if (i < ihi && visible(i, j, s.Lkv, g.wl, g.wr)) {
-                    const float p = exp2f(fmaf(sp, g.scale_log2, -Ls[r]));
-                    const float ds = p * (dpp - Ds[r]);
-#pragma unroll
-                    for (int t = 0; t < DP; ++t) {
-                        dv[t] = fmaf(p, Os[r * D + 4 * t + part], dv[t]);
-                        dk[t] = fmaf(ds, Qs[r * D + 4 * t + part], dk[t]);
-                    }
+                    dv[t] = fmaf(p, Os[r * D + 4 * t + part], dv[t]);
+                    dk[t] = fmaf(ds, Qs[r * D + 4 * t + part], dk[t]);
                 }
             }
         }
     }
-    if (j < s.Lkv) {
-        T *dkrow = row_ptr<T>(a.dk, b, s.kv0 + j, hk);
-        T *dvrow = row_ptr<T>(a.dv, b, s.kv0 + j, hk);
+    // partials of every group: dk and dv [kGroups][kKeys][D]
+    __syncthreads();
+    float *Kp = smem, *Vp = Kp + kGroups * kKeys * D;
 #pragma unroll
-        for (int t = 0; t < DP; ++t) {
-            dkrow[4 * t + part] = from_f32<T>(dk[t] * g.scale);
-            dvrow[4 * t + part] = from_f32<T>(dv[t]);
-        }
+    for (int t = 0; t < DP; ++t) {
+        Kp[(grp * kKeys + kt) * D + 4 * t + part] = dk[t];
+        Vp[(grp * kKeys + kt) * D + 4 * t + part] = dv[t];
     }
+    __syncthreads();
+    for (int e = tid; e < kKeys * D; e += kKvThreads) {
+        const int key = e / D, d = e % D, jj = n0 + key;
+        if (jj >= s.Lkv) continue;
+        float sk = 0.f, sv = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGroups; ++w) {
+            sk += Kp[(w * kKeys + key) * D + d];
+            sv += Vp[(w * kKeys + key) * D + d];
+        }
+        row_ptr<T>(a.dk, b, s.kv0 + jj, hk)[d] = from_f32<T>(sk * g.scale);
+        row_ptr<T>(a.dv, b, s.kv0 + jj, hk)[d] = from_f32<T>(sv);
+    }
+}
+
+template <int D> constexpr size_t fwd_smem() {
+    // Q^T, then the larger of the warps' K / V blocks and their partials
+    return sizeof(float) * (D * kRows + (kSplits * D * kRows + 2 * kSplits * kRows > kSplits * 2 * kBN * D
+                                             ? kSplits * D * kRows + 2 * kSplits * kRows
+                                             : kSplits * 2 * kBN * D));
+}
+template <int D> constexpr size_t dq_smem() {
+    return sizeof(float) * (2 * D * kRows + (kSplits * D * kRows > kSplits * 2 * kBN * D ? kSplits * D * kRows
+                                                                                        : kSplits * 2 * kBN * D));
+}
+template <int D> constexpr size_t dkdv_smem() {
+    constexpr size_t groups = (size_t)kGroups * (2 * kQB * D + 2 * kQB);
+    constexpr size_t parts = (size_t)2 * kGroups * kKeys * D;
+    return sizeof(float) * (groups > parts ? groups : parts);
 }
 
 template <typename T, int D>
 cudaError_t fwd_typed(const FwdArgs &a, int max_lq, cudaStream_t st) {
-    constexpr int BN = (D > 64) ? 16 : 32;
-    const size_t smem = sizeof(float) * (D * (kThreads + 1) + 2 * BN * D);
+    constexpr size_t smem = fwd_smem<D>();
     auto k = simt_fwd_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((max_lq + kThreads - 1) / kThreads, a.g.Hq, a.g.B);
+    dim3 grid((max_lq + kRows - 1) / kRows, a.g.Hq, a.g.B);
     prof_before(st, kProfSimtFwd);
-    k<<<grid, kThreads, smem, st>>>(a);
+    k<<<grid, kSplitThreads, smem, st>>>(a);
     prof_after(st);
     return cudaGetLastError();
 }
@@ -433,8 +541,8 @@ cudaError_t preprocess_any(int dtype, const BwdArgs &a, int rows, cudaStream_t s
 
 template <typename T, int D>
 cudaError_t bwd_typed(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int q_rows, cudaStream_t st) {
-    const size_t smem_dq = sizeof(float) * (2 * D * (kThreads + 1) + 2 * 16 * D);
-    const size_t smem_kv = sizeof(float) * (2 * 32 * D + 2 * 32);
+    constexpr size_t smem_dq = dq_smem<D>();
+    constexpr size_t smem_kv = dkdv_smem<D>();
     auto kq = simt_bwd_dq_kernel<T, D>;
     auto kkv = simt_bwd_dkdv_kernel<T, D>;
     // kernel attributes first, so that a refusal enqueues nothing
@@ -447,16 +555,16 @@ cudaError_t bwd_typed(int dtype, const BwdArgs &a, int max_lq, int max_lkv, int 
         return e;
     if ((e = preprocess_any(dtype, a, q_rows, st)) != cudaSuccess) return e;
     if (max_lq > 0) {
-        dim3 grid((max_lq + kThreads - 1) / kThreads, a.g.Hq, a.g.B);
+        dim3 grid((max_lq + kRows - 1) / kRows, a.g.Hq, a.g.B);
         prof_before(st, kProfSimtBwdDq);
-        kq<<<grid, kThreads, smem_dq, st>>>(a);
+        kq<<<grid, kSplitThreads, smem_dq, st>>>(a);
         prof_after(st);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (max_lkv > 0) {
-        dim3 grid((max_lkv + kThreads / 4 - 1) / (kThreads / 4), a.g.Hkv, a.g.B);
+        dim3 grid((max_lkv + kKeys - 1) / kKeys, a.g.Hkv, a.g.B);
         prof_before(st, kProfSimtBwdDkDv);
-        kkv<<<grid, kThreads, smem_kv, st>>>(a);
+        kkv<<<grid, kKvThreads, smem_kv, st>>>(a);
         prof_after(st);
         return cudaGetLastError();
     }
