@@ -268,3 +268,43 @@ def test_head_dim_256_is_a_16_bit_forward_only(lib):
     st = lib.attn_fwd(ctypes.byref(p32), t, t, t, t, 4096, None)
     assert st == _lib.ATTN_ERR_UNSUPPORTED
     assert lib.attn_fwd(ctypes.byref(_params(D=192)), t, t, t, t, 4096, None) == _lib.ATTN_ERR_UNSUPPORTED
+
+
+def test_invariant_divisor_division_matches_integer_division(tmp_path):
+    """FastDiv (division by a launch-invariant divisor as a multiply and
+    shifts, used by the streaming kernels' index arithmetic) equals unsigned
+    integer division for divisors 1..4096, large and power-of-two divisors,
+    and numerators across the whole 32-bit range.  Host code of the same
+    header the kernels include, compiled with nvcc (no GPU needed)."""
+    import shutil
+    import subprocess
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("no nvcc")
+    src = tmp_path / "fastdiv.cu"
+    src.write_text(
+        '#include <cstdio>\n#include <cstdint>\n#include "common.cuh"\n'
+        "int main() {\n"
+        "    uint32_t ds[4200]; int nd = 0;\n"
+        "    for (uint32_t d = 1; d <= 4096; ++d) ds[nd++] = d;\n"
+        "    const uint32_t big[] = {65535u, 65536u, 65537u, 1000003u, 16777216u, 2147483647u, 2147483648u,\n"
+        "                            3000000019u, 4294967295u};\n"
+        "    for (uint32_t d : big) ds[nd++] = d;\n"
+        "    uint64_t x = 88172645463325252ull; long bad = 0;\n"
+        "    for (int i = 0; i < nd; ++i) {\n"
+        "        const gbattn::FastDiv f(ds[i]);\n"
+        "        const uint32_t edge[] = {0u, 1u, ds[i] - 1u, ds[i], ds[i] + 1u, 4294967295u, 2147483648u};\n"
+        "        for (uint32_t n : edge) bad += f.div(n) != n / ds[i];\n"
+        "        for (int k = 0; k < 2000; ++k) {\n"
+        "            x ^= x << 13; x ^= x >> 7; x ^= x << 17;\n"
+        "            const uint32_t n = (uint32_t)x;\n"
+        "            bad += f.div(n) != n / ds[i];\n"
+        "        }\n"
+        "    }\n"
+        '    printf("%ld\\n", bad);\n'
+        "    return bad != 0;\n}\n")
+    exe = tmp_path / "fastdiv"
+    csrc = os.path.join(ROOT, "scaled_dot_product_03_gb300", "csrc")
+    subprocess.check_call([nvcc, "-std=c++17", "-I", csrc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "0", out.stdout
