@@ -3,7 +3,8 @@
 // One CTA per 128 keys of a (batch, key/value head).  K and V stay in shared
 // memory while the CTA walks the 64-row query blocks of every query head of
 // the group that sees its keys; per block (keys j, queries i):
-//   S^T  = K Q^T,  dP^T = V dO^T          (both operands from shared memory)
+//   S^T  = K Q^T                          (K from TMEM, Q from shared memory)
+//   dP^T = V dO^T                         (both operands from shared memory)
 //   P^T  = exp(scale S^T - LSE)           recomputed from the forward's LSE
 //   dS^T = P^T o (dP^T - delta)           delta_i = <dO_i, O_i> (preprocess)
 //   dV  += P^T dO                         (P^T from TMEM)
@@ -19,9 +20,9 @@
 // small kernel scales and converts the sums at the end.  The order of those fp32 additions depends on scheduling, so
 // dQ is reproducible only to rounding; dK and dV are owned by one CTA each.
 //
-// Warp roles (448 threads): warps 0-7 compute P and dS (thread = key row;
-// warps 0-3 take query columns 0-31 of the block, warps 4-7 columns 32-63)
-// and write dK / dV at the end (staged in the then idle K / V tiles and
+// Warp roles (448 threads): warps 0-7 copy K into TMEM, compute P and dS
+// (thread = key row; warps 0-3 take query columns 0-31 of the block, warps
+// 4-7 columns 32-63) and write dK / dV at the end (staged in the then idle K / V tiles and
 // written with TMA stores); warp 8 issues TMA loads; warp 9 allocates
 // TMEM and issues the MMAs; warps 10-13 drain dQ^T from TMEM (thread = head
 // dim) into shared memory and issue the reductions, warp w owning head dims
@@ -29,7 +30,10 @@
 // and one 64 x 32 fp32 staging box.
 //
 // TMEM columns (512): dK 0-127, dV 128-255, S^T / P^T 256-319, dP^T / dS^T
-// in two buffers 320-383 and 384-447, dQ^T 448-511.  Shared memory: K, V
+// 320-383, dQ^T 384-447, and K 448-511 (bf16 pairs, written once by the
+// compute warps) as the A operand of S^T: operands read from TMEM do not
+// use the shared-memory port, which the five products' shared-memory
+// operands and the warps' own traffic otherwise fill.  Shared memory: K, V
 // (32 KB each), three stages of Q and dO (16 KB each), two dS^T buffers
 // (16 KB each), the dQ staging boxes (32 KB) and the per-stage LSE / delta.
 #include <type_traits>
@@ -73,13 +77,13 @@ constexpr int kBarOff = kStatOff + QS * BQ * 2 * 4;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;      // + barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kTmDK = 0, kTmDV = 128, kTmS = 256, kTmDP = 320, kTmDQ = 448;
+constexpr uint32_t kTmDK = 0, kTmDV = 128, kTmS = 256, kTmDP = 320, kTmDQ = 384, kTmK = 448;
 
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[QS], q_empty[QS];
-    uint64_t s_full, p_full;
-    uint64_t dp_full[2], ds_full[2];
+    uint64_t k_tmem, s_full, p_full;
+    uint64_t dp_full, ds_full;
     uint64_t dq_full, dq_free, acc_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -138,12 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar.q_full[i], 32);
             mbar_init(&bar.q_empty[i], 1);
         }
+        mbar_init(&bar.k_tmem, kCompute);
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.p_full, kCompute);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar.dp_full[i], 1);
-            mbar_init(&bar.ds_full[i], kCompute);
-        }
+        mbar_init(&bar.dp_full, 1);
+        mbar_init(&bar.ds_full, kCompute);
         mbar_init(&bar.dq_full, 1);
         mbar_init(&bar.dq_free, kDrain);
         mbar_init(&bar.acc_done, 1);
@@ -220,8 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA
         // Per block t: dV_t (once P_t is written), S^T_{t+1} (its TMEM held
         // P_t, read by dV_t just before: MMAs of one thread execute in issue
-        // order), dP^T_{t+1} (into the other dP buffer), then dK_t and dQ^T_t
-        // once dS_t is in TMEM and shared memory.
+        // order), then, once dS_t is in TMEM and shared memory, dK_t,
+        // dP^T_{t+1} (its TMEM held dS^T_t, read by dK_t just before) and
+        // dQ^T_t.
         // The whole warp runs the loop (waits, operand descriptors) in step;
         // one elected lane issues each group of MMAs and its commit.
         if (n_it > 0) {
@@ -230,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idQ = idesc_f16(D, BQ, kBf16, 1, 1);    // dQ^T: A = K, B = dS^T, MN-major
             const uint32_t sQ = smem_u32(smem + kQOff), sDO = smem_u32(smem + kDOOff);
             const uint32_t sDS = smem_u32(smem + kDSOff);
-            const uint64_t dK = smem_desc_sw128(smem_u32(smem + kKOff), 16, 1024);
             const uint64_t dV = smem_desc_sw128(smem_u32(smem + kVOff), 16, 1024);
             // K as the MN-major A operand of dQ^T (M = head dim, two 64-wide atoms)
             const uint64_t dKm = smem_desc_sw128(smem_u32(smem + kKOff), BK * 128, 1024);
@@ -242,26 +245,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_s = [&](int t) {
                 const uint64_t db = smem_desc_sw128(sQ + (t % QS) * kQTile, 16, 1024);
                 if (elect_one()) {
+                    // k-step kk of K: head dims [16 kk, 16 kk + 16) = TMEM columns [8 kk, 8 kk + 8)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + kTmS, desc_add(dK, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP,
-                               kk > 0);
+                        mma_ts(tmem + kTmS, tmem + kTmK + kk * 8, desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
                     mma_commit(&bar.s_full);
                 }
                 __syncwarp();
             };
             auto issue_dp = [&](int t) {
                 const uint64_t db = smem_desc_sw128(sDO + (t % QS) * kQTile, 16, 1024);
-                const uint32_t dst = tmem + kTmDP + (t & 1) * BQ;
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(dst, desc_add(dV, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
-                    mma_commit(&bar.dp_full[t & 1]);
+                        mma_ss(tmem + kTmDP, desc_add(dV, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP,
+                               kk > 0);
+                    mma_commit(&bar.dp_full);
                 }
                 __syncwarp();
             };
-            bool ok = wait(&bar.kv_full, 0, 0xd0) && wait(&bar.q_full[0], 0, 0xd1);
+            bool ok = wait(&bar.kv_full, 0, 0xd0) && wait(&bar.k_tmem, 0, 0xd6) && wait(&bar.q_full[0], 0, 0xd1);
             if (ok) {
                 issue_s(0);
                 issue_dp(0);
@@ -284,20 +287,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (next) {
                     if (!(ok = wait(&bar.q_full[(t + 1) % QS], ((t + 1) / QS) & 1, 0xd3))) break;
                     issue_s(t + 1);
-                    issue_dp(t + 1);
                 }
-                if (!(ok = wait(&bar.ds_full[t & 1], (t >> 1) & 1, 0xd4))) break;
+                if (!(ok = wait(&bar.ds_full, t & 1, 0xd4))) break;
                 // dS^T_t: A of dK from TMEM (packed over dP^T_t), MN-major B of
                 // dQ^T from shared memory (N = queries)
                 const uint64_t dSm = smem_desc_sw128(sDS + (t & 1) * kDSTile, BK * 128, 1024);
-                const uint32_t tds = tmem + kTmDP + (t & 1) * BQ;
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < BQ / 16; ++kk)
-                        mma_ts(tmem + kTmDK, tds + pcol(kk), desc_add(dQm, kk * 16 * 128), idKV, kk > 0 ? 1u : acc0);
+                        mma_ts(tmem + kTmDK, tmem + kTmDP + pcol(kk), desc_add(dQm, kk * 16 * 128), idKV,
+                               kk > 0 ? 1u : acc0);
                     mma_commit(&bar.q_empty[st]);
                 }
                 __syncwarp();
+                if (next) issue_dp(t + 1);
                 if (t > 0 && !(ok = wait(&bar.dq_free, (t - 1) & 1, 0xd5))) break;
                 if (elect_one()) {
 #pragma unroll
@@ -321,7 +324,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sDSrow = smem_u32(smem + kDSOff) + j * 128;
         const float c2 = g.scale_log2;
         bool ok = true;
-        for (int t = 0; t < n_it; ++t) {
+        if (n_it > 0) {
+            // K row j into TMEM as bf16 pairs: this half's head dims [64 half,
+            // 64 half + 64) are atom `half` of the swizzled tile (16-byte chunk
+            // c of the row at c ^ (j % 8)), TMEM columns [32 half, 32 half + 32)
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_full, 0, wd, 0xe3));
+            if (ok) {
+                const uint8_t *krow = smem + kKOff + half * (BK * 128) + j * 128;
+                uint32_t kr[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(krow + ((c ^ (j & 7)) << 4));
+                    kr[4 * c] = x.x;
+                    kr[4 * c + 1] = x.y;
+                    kr[4 * c + 2] = x.z;
+                    kr[4 * c + 3] = x.w;
+                }
+                tmem_st32(tmem + kTmK + half * 32 + lane_off, kr);
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            mbar_arrive(&bar.k_tmem);
+        }
+        for (int t = 0; ok && t < n_it; ++t) {
             const int st = t % QS;
             const int i0 = ilo + (t % nqb) * BQ + c0;  // first query row of this half
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, t & 1, wd, 0xe0));
@@ -368,13 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bar.p_full);
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full[t & 1], (t >> 1) & 1, wd, 0xe1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.dp_full, t & 1, wd, 0xe1));
             if (!ok) break;
             tc_fence_after();
             // dS^T_t packed over dP^T_t in TMEM (A of dK) and into shared memory
             // (B of dQ^T; the buffer was last read by dQ^T_{t-2}, issued
             // before dP^T_t, whose completion we saw)
-            const uint32_t tDP = tmem + kTmDP + (t & 1) * BQ + c0 + lane_off;
+            const uint32_t tDP = tmem + kTmDP + c0 + lane_off;
             uint32_t pk[16];
             {
                 uint32_t dr[32];
@@ -398,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bar.ds_full[t & 1]);
+            mbar_arrive(&bar.ds_full);
         }
         // epilogue: dK (scaled) from warps 0-3, dV from warps 4-7
         if (ok && n_it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.acc_done, 0, wd, 0xe2));
