@@ -4,7 +4,8 @@
 // (query, key) pair, dV and dK owned by the CTA, each block's share of dQ
 // added into an fp32 accumulator), laid out for D = 64, where TMEM has room
 // for 128-query blocks and an untransposed dQ:
-//   S^T  = K Q^T,  dP^T = V dO^T          (M = 128 keys, N = 128 queries)
+//   S^T  = K Q^T,  dP^T = V dO^T          (M = 128 keys, N = 128 queries;
+//                                         K and V from TMEM)
 //   P^T  = exp(scale S^T - LSE),  dS^T = P^T o (dP^T - delta)
 //   dV  += P^T dO,  dK += dS^T Q          (P^T, dS^T from TMEM)
 //   dQ   = dS K                           (M = 128 queries; dS from shared
@@ -12,14 +13,16 @@
 // so every product runs with M = 128 and the dQ drain holds query rows
 // (thread = query row), which it writes as row-major boxes.
 //
-// One CTA per 128 keys of a (batch, key/value head); warps 0-7 compute P and
-// dS (thread = key row; warps 0-3 take query columns 0-63 of the block,
-// warps 4-7 columns 64-127) and write dK / dV; warp 8 loads; warp 9 issues
+// One CTA per 128 keys of a (batch, key/value head); warps 0-7 copy K
+// (warps 0-3) and V (warps 4-7) into TMEM, compute P and dS (thread = key
+// row; warps 0-3 take query columns 0-63 of the block, warps 4-7 columns
+// 64-127) and write dK / dV; warp 8 loads; warp 9 issues
 // the MMAs (the whole warp runs the loop, an elected lane issues); warps
 // 10-13 drain dQ (warp w: query rows [32 (w % 4), 32 (w % 4) + 32)).
 //
-// TMEM columns (448 used of 512): dK 0-63, dV 64-127, S^T / P^T 128-255,
-// dP^T / dS^T 256-383, dQ 384-447.  MMA order per block t: dV_t, S^T_{t+1},
+// TMEM columns (512): dK 0-63, dV 64-127, S^T / P^T 128-255, dP^T / dS^T
+// 256-383, dQ 384-447, K 448-479 and V 480-511 (bf16 pairs, the A operands
+// of S^T and dP^T, which then take no shared-memory bandwidth).  MMA order per block t: dV_t, S^T_{t+1},
 // dK_t, dQ_t, dP^T_{t+1}; dP^T_{t+1} overwrites dS^T_t after dK_t read it and
 // is issued after dQ_t read dS_t from shared memory, so one dS^T buffer
 // suffices (its next writer waits for dP^T_{t+1}).  Shared memory: K, V,
@@ -66,12 +69,12 @@ constexpr int kBarOff = kStatOff + QS * BQ * 2 * 4;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kTmDK = 0, kTmDV = 64, kTmS = 128, kTmDP = 256, kTmDQ = 384;
+constexpr uint32_t kTmDK = 0, kTmDV = 64, kTmS = 128, kTmDP = 256, kTmDQ = 384, kTmK = 448, kTmV = 480;
 
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[QS], q_empty[QS];
-    uint64_t s_full, p_full, dp_full, ds_full;
+    uint64_t kv_tmem, s_full, p_full, dp_full, ds_full;
     uint64_t dq_full, dq_free, acc_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar.q_full[i], 32);
             mbar_init(&bar.q_empty[i], 1);
         }
+        mbar_init(&bar.kv_tmem, kCompute);
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.p_full, kCompute);
         mbar_init(&bar.dp_full, 1);
@@ -200,8 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idKV = idesc_f16(BK, D, kBf16, 0, 1);   // dV, dK: B = dO / Q, MN-major
             constexpr uint32_t idQ = idesc_f16(BQ, D, kBf16, 1, 1);    // dQ: A = dS, B = K, MN-major
             const uint32_t sQ = smem_u32(smem + kQOff), sDO = smem_u32(smem + kDOOff);
-            const uint64_t dK = smem_desc_sw128(smem_u32(smem + kKOff), 16, 1024);
-            const uint64_t dV = smem_desc_sw128(smem_u32(smem + kVOff), 16, 1024);
             const uint64_t dKm = smem_desc_sw128(smem_u32(smem + kKOff), BK * 128, 1024);  // B of dQ
             const uint64_t dSm = smem_desc_sw128(smem_u32(smem + kDSOff), BK * 128, 1024); // A of dQ
             auto wait = [&](uint64_t *bb, uint32_t ph, unsigned code) {
@@ -212,10 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_s = [&](int t) {
                 const uint64_t db = smem_desc_sw128(sQ + (t % QS) * kQTile, 16, 1024);
                 if (elect_one()) {
+                    // k-step kk: head dims [16 kk, 16 kk + 16) = TMEM columns [8 kk, 8 kk + 8)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + kTmS, desc_add(dK, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP,
-                               kk > 0);
+                        mma_ts(tmem + kTmS, tmem + kTmK + kk * 8, desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
                     mma_commit(&bar.s_full);
                 }
                 __syncwarp();
@@ -225,13 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + kTmDP, desc_add(dV, kmaj_off(kk, BK)), desc_add(db, kmaj_off(kk, BQ)), idSP,
-                               kk > 0);
+                        mma_ts(tmem + kTmDP, tmem + kTmV + kk * 8, desc_add(db, kmaj_off(kk, BQ)), idSP, kk > 0);
                     mma_commit(&bar.dp_full);
                 }
                 __syncwarp();
             };
-            bool ok = wait(&bar.kv_full, 0, 0xd8) && wait(&bar.q_full[0], 0, 0xd9);
+            bool ok = wait(&bar.kv_full, 0, 0xd8) && wait(&bar.kv_tmem, 0, 0xde) && wait(&bar.q_full[0], 0, 0xd9);
             if (ok) {
                 issue_s(0);
                 issue_dp(0);
@@ -290,7 +291,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sDSrow = smem_u32(smem + kDSOff) + half * (BK * 128) + j * 128;
         const float c2 = g.scale_log2;
         bool ok = true;
-        for (int t = 0; t < n_it; ++t) {
+        if (n_it > 0) {
+            // row j of K (warps 0-3) or V (warps 4-7) into TMEM as bf16 pairs:
+            // 16-byte chunk c of the swizzled row sits at c ^ (j % 8)
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar.kv_full, 0, wd, 0xeb));
+            if (ok) {
+                const uint8_t *row = smem + (half == 0 ? kKOff : kVOff) + j * 128;
+                uint32_t kr[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(row + ((c ^ (j & 7)) << 4));
+                    kr[4 * c] = x.x;
+                    kr[4 * c + 1] = x.y;
+                    kr[4 * c + 2] = x.z;
+                    kr[4 * c + 3] = x.w;
+                }
+                tmem_st32(tmem + (half == 0 ? kTmK : kTmV) + lane_off, kr);
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            mbar_arrive(&bar.kv_tmem);
+        }
+        for (int t = 0; ok && t < n_it; ++t) {
             const int st = t % QS;
             const int i0 = ilo + (t % nqb) * BQ + c0;
             ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full, t & 1, wd, 0xe8));
