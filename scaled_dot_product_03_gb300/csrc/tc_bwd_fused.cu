@@ -22,12 +22,13 @@
 //
 // Warp roles (448 threads): warps 0-7 copy K into TMEM, compute P and dS
 // (thread = key row; warps 0-3 take query columns 0-31 of the block, warps
-// 4-7 columns 32-63) and write dK / dV at the end (staged in the then idle K / V tiles and
-// written with TMA stores); warp 8 issues TMA loads; warp 9 allocates
-// TMEM and issues the MMAs; warps 10-13 drain dQ^T from TMEM (thread = head
-// dim) into shared memory and issue the reductions, warp w owning head dims
-// [32 (w % 4), 32 (w % 4) + 32), which is the TMEM lane quarter it may read,
-// and one 64 x 32 fp32 staging box.
+// 4-7 columns 32-63) and write dK at the end; warp 8 issues TMA loads; warp
+// 9 allocates TMEM and issues the MMAs; warps 10-13 drain dQ^T from TMEM
+// (thread = head dim) into shared memory and issue the reductions, warp w
+// owning head dims [32 (w % 4), 32 (w % 4) + 32), which is the TMEM lane
+// quarter it may read, and one 64 x 32 fp32 staging box, and write dV at
+// the end.  dK and dV leave in parallel, each warp staging 32-row boxes in
+// the then idle K / V tiles for TMA stores.
 //
 // TMEM columns (512): dK 0-127, dV 128-255, S^T / P^T 256-319, dP^T / dS^T
 // 320-383, dQ^T 384-447, and K 448-511 (bf16 pairs, written once by the
@@ -425,80 +426,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&bar.ds_full);
         }
-        // epilogue: dK (scaled) from warps 0-3, dV from warps 4-7
+        // epilogue: dK (scaled), warp w taking rows [32 (w % 4), 32 (w % 4) +
+        // 32) and head dims [64 half, 64 half + 64); the drain warps write dV
+        // at the same time.  Once every MMA has completed the K tile is idle:
+        // each warp stages its 32 x 64 box there (the tile's own 128B-swizzled
+        // layout; the box starts at a 1 KB boundary, so row j's swizzle phase
+        // is j % 8) and writes it with a TMA store, which drops rows past a
+        // dense tensor's end.  A THD tile that ends inside the tensor would
+        // spill into the next sequence, so it is written row by row instead.
+        // With split query heads the row is this split's fp32 partial,
+        // summed by a second kernel.
         if (ok && n_it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.acc_done, 0, wd, 0xe2));
         tc_fence_after();
-        const float mul = half == 0 ? g.scale : 1.f;
-        const uint32_t base = tmem + (half == 0 ? kTmDK : kTmDV) + lane_off;
-        // The K and V tiles are idle once every MMA has completed: stage the
-        // tile there (same 128B-swizzled layout as the loads) and write it
-        // with TMA stores, which drop rows past a dense tensor's end.  A THD
-        // tile that ends inside the tensor would spill into the next
-        // sequence, so it is written row by row instead.  With split query
-        // heads the row is this split's fp32 partial, summed by a second
-        // kernel.
+        const uint32_t base = tmem + kTmDK + half * 64 + lane_off;
+        auto load_dk = [&](int cc, uint32_t (&v)[32]) {
+            if (n_it > 0) {
+                tmem_ld32(base + cc * 32, v);  // warp-wide: every lane loads
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+        };
         if (a.dkv_part) {
             const int64_t krow = (g.thd ? 0 : (int64_t)b * g.Skv) + s.kv0 + key;
             const int64_t nrows = g.thd ? g.Skv : (int64_t)g.B * g.Skv;
-            float *dst = a.dkv_part + (((int64_t)(sp * 2 + half) * nrows + krow) * g.Hkv + hk) * D;
+            float *dst = a.dkv_part + (((int64_t)(sp * 2) * nrows + krow) * g.Hkv + hk) * D + half * 64;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t v[32];
-                if (n_it > 0) {
-                    tmem_ld32(base + cc * 32, v);  // warp-wide: every lane loads
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
+                load_dk(cc, v);
                 if (j < nkeys) store_f32_row32(dst + cc * 32, v);
             }
         } else if (!g.thd || nkeys == BK) {
-            uint8_t *stage = smem + (half == 0 ? kKOff : kVOff);
-            const uint32_t srow = smem_u32(stage) + j * 128;
+            uint8_t *boxp = smem + kKOff + half * (BK * 128) + (warp % 4) * 4096;
+            const uint32_t srow = smem_u32(boxp) + lane * 128;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t v[32];
-                if (n_it > 0) {
-                    tmem_ld32(base + cc * 32, v);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
+                load_dk(cc, v);
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    w[e] = pack2<T>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-                // 16-byte chunks 4 cc .. 4 cc + 3 of the row: atom (chunk / 8),
-                // position (chunk % 8) ^ (row % 8) inside the atom's row
+                    w[e] = pack2<T>(__uint_as_float(v[2 * e]) * g.scale, __uint_as_float(v[2 * e + 1]) * g.scale);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int c16 = cc * 4 + q;
-                    st_shared_v4(srow + (c16 / 8) * (BK * 128) + ((uint32_t)((c16 % 8) ^ (j & 7)) << 4), w[4 * q],
-                                 w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    const int c16 = cc * 4 + q;  // 16-byte chunk of the box row
+                    st_shared_v4(srow + ((uint32_t)(c16 ^ (lane & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                                 w[4 * q + 3]);
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1 + half, 128);
-            if (warp % 4 == 0 && lane == 0) {
-                const CUtensorMap *m = half == 0 ? &tm_dk : &tm_dv;
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) tma_store_4d(m, stage + c * BK * 128, c * 64, s.kv0 + n0, hk, cb);
+            __syncwarp();
+            if (lane == 0 && (warp % 4) * 32 < nkeys) {
+                tma_store_4d(&tm_dk, boxp, half * 64, s.kv0 + n0 + (warp % 4) * 32, hk, cb);
                 bulk_commit();
                 bulk_wait_read0();  // the copy has read the staging before the CTA exits
             }
+            __syncwarp();
         } else {
-            const MutView &ov = half == 0 ? a.dk : a.dv;
-            T *dstp = (T *)ov.ptr + (int64_t)b * ov.sb + (int64_t)(s.kv0 + key) * ov.ss + (int64_t)hk * ov.sh;
+            T *dstp = (T *)a.dk.ptr + (int64_t)b * a.dk.sb + (int64_t)(s.kv0 + key) * a.dk.ss + (int64_t)hk * a.dk.sh +
+                      half * 64;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t v[32];
-                if (n_it > 0) {
-                    tmem_ld32(base + cc * 32, v);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
-                if (j < nkeys && cc * 32 < g.D) store_row32<T>(dstp + cc * 32, v, mul);
+                load_dk(cc, v);
+                if (j < nkeys && half * 64 + cc * 32 < g.D) store_row32<T>(dstp + cc * 32, v, g.scale);
             }
         }
     } else if (warp >= kDrainWarp0) {
@@ -536,8 +528,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_commit();
             }
         }
-        // the reductions must have read their boxes before the CTA's shared
-        // memory goes away (their additions complete with the grid)
+        // dV rows [32 qd, 32 qd + 32), all head dims, once every MMA has
+        // completed: staged as two 32 x 64 boxes in the then idle V tile
+        // (swizzle phase lane % 8, as for dK) and written with TMA stores; THD
+        // tiles ending inside the tensor row by row; with split query heads
+        // this split's fp32 partial.
+        if (ok && n_it > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar.acc_done, 0, wd, 0xf2));
+        tc_fence_after();
+        {
+            const int j = qd * 32 + lane;  // key within the tile
+            const uint32_t base = tmem + kTmDV + lane_off;
+            auto load_dv = [&](int cc, uint32_t (&v)[32]) {
+                if (n_it > 0) {
+                    tmem_ld32(base + cc * 32, v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+            };
+            if (a.dkv_part) {
+                const int64_t krow = (g.thd ? 0 : (int64_t)b * g.Skv) + s.kv0 + n0 + j;
+                const int64_t nrows = g.thd ? g.Skv : (int64_t)g.B * g.Skv;
+                float *dst = a.dkv_part + (((int64_t)(sp * 2 + 1) * nrows + krow) * g.Hkv + hk) * D;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    load_dv(cc, v);
+                    if (j < nkeys) store_f32_row32(dst + cc * 32, v);
+                }
+            } else if (!g.thd || nkeys == BK) {
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    load_dv(cc, v);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) w[e] = pack2<T>(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int c16 = cc * 4 + q;  // 16-byte chunk of the row: atom c16 / 8
+                        st_shared_v4(smem_u32(smem + kVOff) + (c16 / 8) * (BK * 128) + qd * 4096 + lane * 128 +
+                                         ((uint32_t)((c16 % 8) ^ (lane & 7)) << 4),
+                                     w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && qd * 32 < nkeys) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_store_4d(&tm_dv, smem + kVOff + c * (BK * 128) + qd * 4096, c * 64, s.kv0 + n0 + qd * 32, hk,
+                                     cb);
+                    bulk_commit();
+                }
+                __syncwarp();
+            } else {
+                T *dstp = (T *)a.dv.ptr + (int64_t)b * a.dv.sb + (int64_t)(s.kv0 + n0 + j) * a.dv.ss + (int64_t)hk * a.dv.sh;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    load_dv(cc, v);
+                    if (j < nkeys && cc * 32 < g.D) store_row32<T>(dstp + cc * 32, v, 1.f);
+                }
+            }
+        }
+        // the copies must have read their boxes before the CTA's shared
+        // memory goes away (the reductions' additions complete with the grid)
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
     }
@@ -687,8 +743,9 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
         if ((e = make_tmap_16bit(&tv, a.v.ptr, dt, dk, sv, BK)) != cudaSuccess) return e;
         if ((e = make_tmap_16bit(&tdo, a.dout.ptr, dt, dq, sd, BQ)) != cudaSuccess) return e;
         if ((e = make_tmap_f32_acc(&tacc, a.dq_acc, D, acc_rows, acc_heads, 32, BQ)) != cudaSuccess) return e;
-        if ((e = make_tmap_16bit(&tgk, a.dk.ptr, dt, dk, sgk, BK)) != cudaSuccess) return e;
-        if ((e = make_tmap_16bit(&tgv, a.dv.ptr, dt, dk, sgv, BK)) != cudaSuccess) return e;
+        // dK / dV leave in 32-row boxes, one per TMEM lane quarter
+        if ((e = make_tmap_16bit(&tgk, a.dk.ptr, dt, dk, sgk, 32)) != cudaSuccess) return e;
+        if ((e = make_tmap_16bit(&tgv, a.dv.ptr, dt, dk, sgv, 32)) != cudaSuccess) return e;
         auto kern = tc_bwd_fused_kernel<T>;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
             cudaSuccess)
