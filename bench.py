@@ -471,7 +471,8 @@ def _time_steps(one, n, flush=None):
 
 def workload_lines(gb, inputs, dev, peak):
     """fwd+bwd TFLOP/s on the packed THD workload (16 causal sequences of
-    U[128, 4096] tokens, 32 query heads over 8 KV heads, D=128), on a causal
+    U[128, 4096] tokens, 32 query heads over 8 KV heads, D=128), on that
+    workload under the emulated context-parallel ring (CP = 4), on a causal
     sliding window (1023, 0) over S=16384, and the S=1024 sweep point with
     the L2 flushed before every step."""
     import torch
@@ -507,7 +508,38 @@ def workload_lines(gb, inputs, dev, peak):
     out["varlen_thd"] = line("bf16 THD causal, %d sequences U[128,4096] (T=%d), Hq=32 Hkv=8 "
                              "D=128" % (len(lens), sum(lens)), 4.0 * 128 * nvis,
                              10.0 * 128 * nvis, _time_steps(fwd, 20), _time_steps(step, 20))
-    del d, fwd, step
+    del fwd, step
+
+    # The same batch under the load-balanced context-parallel split, CP = 4,
+    # every rank's ring emulated on this GPU: each sequence padded to a
+    # multiple of 2 CP rows, the ring forward (pair attentions merged by LSE)
+    # and its backward (pair backward with the merged O and LSE, fp32 sums).
+    # The ring plans its calls on the host from cu_seqlens every call.
+    from scaled_dot_product_03_gb300 import cp
+    cp_size = 4
+    pads = [0]
+    for L in lens:
+        pads.append(pads[-1] + -(-L // (2 * cp_size)) * (2 * cp_size))
+    rows = torch.cat([torch.arange(pads[b], pads[b] + L) for b, L in enumerate(lens)]).to(dev)
+
+    def padded(t):
+        z = torch.zeros((pads[-1],) + tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+        z[rows] = t
+        return z
+    qp, kp, vp, dop = padded(d.q), padded(d.k), padded(d.v), padded(d.dout)
+    pad_d = torch.tensor(pads, dtype=torch.int32, device=dev)
+
+    def cp_fwd():
+        return cp.ring_attention_fwd(qp, kp, vp, d.cu_seqlens_q, pad_d, cp_size, causal=True, scale=d.scale)
+
+    def cp_step():
+        o_r, l_r = cp_fwd()
+        cp.ring_attention_bwd(dop, qp, kp, vp, o_r, l_r, d.cu_seqlens_q, pad_d, cp_size, causal=True,
+                              scale=d.scale)
+    out["cp_ring_thd"] = line("the THD workload above under CP=4 (sequences padded to multiples of 8 rows, "
+                              "T=%d), every rank's ring emulated on one GPU" % pads[-1], 4.0 * 128 * nvis,
+                              10.0 * 128 * nvis, _time_steps(cp_fwd, 5), _time_steps(cp_step, 5))
+    del d, qp, kp, vp, dop
 
     B, S, H, D, win = 1, 16384, 16, 128, (1023, 0)
     d = inputs.dense(B, S, H, D, window=win, seed=3, dout_seed=4).to(dev)

@@ -263,6 +263,41 @@ GBATTN_API attn_status attn_thd_partitioned_indices(const int32_t *cu_seqlens_pa
                                          int32_t *indices, attn_stream_t stream);
 
 /*
+ * Gradient sums of the context-parallel ring ("[PyTorch] Add support for
+ * cuDNN FusedAttention + THD + CP", which runs THD + CP through the fused
+ * attention kernels).  The pages do not spell out the ring's backward; the
+ * library takes its plainest reading, the derivative of the merged result:
+ * each ring step's attention backward, called with the merged O and LSE,
+ * gives the step's share of dQ (rows of the rank's query chunk) and of dK,
+ * dV (rows of the key/value chunk it holds), and each gradient is the sum
+ * of its shares.
+ * These two calls add the shares in fp32 and write the sums out.
+ *
+ * attn_thd_accumulate: acc[t, h, :] += src[t, h, :] (accumulate = 1) or
+ * acc[t, h, :] = src[t, h, :] (accumulate = 0, for a first share) for every
+ * head h < H and every token row t inside a sequence (rows
+ * cu_seqlens_padded[b] + i, i < cu_seqlens[b+1] - cu_seqlens[b];
+ * cu_seqlens_padded NULL: rows cu_seqlens[b] + i).  Other rows of acc are
+ * left as they are.
+ * attn_thd_store: dst[t, h, :] = acc[t, h, :] in the element type for rows
+ * inside a sequence, and 0 for every other row t < T.
+ * src / dst: THD views [T, H, D] of element type dtype (fp16, bf16 or fp32;
+ * element (t, h, d) at ptr + t*stride[1] + h*stride[2] + d, stride[3] = 1).
+ * acc: fp32 [T, H, D], contiguous.  D: a multiple of 8 up to 256.  Pointers
+ * (device) and strides must be 16-byte aligned; cu_seqlens (and
+ * cu_seqlens_padded) are device int32 with B + 1 entries.  T = 0 or H = 0
+ * does nothing.  Returns INVALID_ARG (nothing enqueued) on bad sizes, NULL
+ * pointers or misalignment.
+ */
+GBATTN_API attn_status attn_thd_accumulate(attn_dtype dtype, int T, int H, int D, attn_tensor src,
+                                           float *acc, int accumulate, const int32_t *cu_seqlens,
+                                           const int32_t *cu_seqlens_padded, int B,
+                                           attn_stream_t stream);
+GBATTN_API attn_status attn_thd_store(attn_dtype dtype, int T, int H, int D, const float *acc,
+                                      attn_tensor dst, const int32_t *cu_seqlens,
+                                      const int32_t *cu_seqlens_padded, int B, attn_stream_t stream);
+
+/*
  * Per-launch timing, for benchmarks and profilers.  After
  * attn_profile_begin(n) the calling thread's next (at most n) kernel
  * launches by this library are each bracketed by two CUDA events recorded
@@ -284,7 +319,8 @@ enum {
     ATTN_KERNEL_BWD_FUSED = 8,      /* tensor-core single-pass dK, dV, dQ share */
     ATTN_KERNEL_BWD_DQ_CONVERT = 9, /* fp32 dq accumulator -> dq */
     ATTN_KERNEL_MERGE_BWD = 10,     /* backward of the LSE merge */
-    ATTN_KERNEL_BWD_DKV_REDUCE = 11 /* dK, dV summed over split query heads */
+    ATTN_KERNEL_BWD_DKV_REDUCE = 11, /* dK, dV summed over split query heads */
+    ATTN_KERNEL_THD_ROWS = 12        /* THD gradient sums of the context-parallel ring */
 };
 GBATTN_API attn_status attn_profile_begin(int max_launches);
 GBATTN_API int attn_profile_read(float *ms, int *kind, int capacity);

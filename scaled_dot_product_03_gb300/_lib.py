@@ -23,10 +23,10 @@ EXPORTS = ("attn_fwd", "attn_bwd_workspace_size", "attn_bwd", "attn_merge_lse",
            "attn_last_error_string", "attn_check_device_error", "attn_set_watchdog_ns",
            "attn_watchdog_selftest", "attn_profile_begin", "attn_profile_read",
            "attn_bwd_noalloc", "attn_bwd_dlse", "attn_merge_lse_bwd",
-           "attn_thd_partitioned_indices")
+           "attn_thd_partitioned_indices", "attn_thd_accumulate", "attn_thd_store")
 KERNEL_KINDS = {0: "fwd", 1: "bwd_preprocess", 2: "bwd_dkdv", 3: "bwd_dq", 4: "merge",
                 5: "simt_fwd", 6: "simt_bwd_dq", 7: "simt_bwd_dkdv", 8: "bwd_fused",
-                9: "bwd_dq_convert", 10: "merge_bwd", 11: "bwd_dkv_reduce"}
+                9: "bwd_dq_convert", 10: "merge_bwd", 11: "bwd_dkv_reduce", 12: "thd_rows"}
 NOALLOC_SCRATCH_BYTES = 64 << 20  # GBATTN_NOALLOC_SCRATCH_BYTES
 
 
@@ -86,6 +86,11 @@ def load(path: str = LIB_PATH):
         lib.attn_thd_partitioned_indices.argtypes = [ctypes.c_void_p, i32, i32, i32, i32,
                                                      ctypes.c_void_p, S]
         lib.attn_thd_partitioned_indices.restype = i32
+        lib.attn_thd_accumulate.argtypes = [i32, i32, i32, i32, T, f32p, i32, ctypes.c_void_p,
+                                            ctypes.c_void_p, i32, S]
+        lib.attn_thd_accumulate.restype = i32
+        lib.attn_thd_store.argtypes = [i32, i32, i32, i32, f32p, T, ctypes.c_void_p, ctypes.c_void_p, i32, S]
+        lib.attn_thd_store.restype = i32
         lib.attn_last_error_string.argtypes = []
         lib.attn_last_error_string.restype = ctypes.c_char_p
         lib.attn_check_device_error.argtypes = [S]

@@ -540,6 +540,47 @@ attn_status attn_thd_partitioned_indices(const int32_t *cu_seqlens_padded, int B
     return ATTN_OK;
 }
 
+namespace {
+
+attn_status thd_rows(const char *name, attn_dtype dtype, int T, int H, int D, attn_tensor v, float *acc,
+                     const int32_t *cu, const int32_t *pad, int B, int mode, attn_stream_t stream) {
+    t_error.clear();
+    if (dtype != ATTN_F16 && dtype != ATTN_BF16 && dtype != ATTN_F32)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: unknown dtype %d", name, (int)dtype);
+    if (T < 0 || H < 0 || B < 0) return fail(ATTN_ERR_INVALID_ARG, "%s: negative size", name);
+    if (D < 8 || D > 256 || D % 8) return fail(ATTN_ERR_INVALID_ARG, "%s: D = %d is not a multiple of 8 in [8, 256]", name, D);
+    if ((int64_t)T * H == 0) return ATTN_OK;
+    if (B < 1 || !cu || !v.ptr || !acc) return fail(ATTN_ERR_INVALID_ARG, "%s: need B >= 1 and non-NULL pointers", name);
+    const int64_t elt = dtype == ATTN_F32 ? 4 : 2;
+    if (v.stride[3] != 1) return fail(ATTN_ERR_INVALID_ARG, "%s: the d stride must be 1", name);
+    if ((uintptr_t)v.ptr % 16 || (uintptr_t)acc % 16 || (v.stride[1] * elt) % 16 || (v.stride[2] * elt) % 16)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: pointers and strides must be 16-byte aligned", name);
+    MutView mv;
+    mv.ptr = v.ptr;
+    mv.sb = 0;
+    mv.ss = v.stride[1];
+    mv.sh = v.stride[2];
+    cudaError_t e = launch_thd_rows((int)dtype, mode, T, H, D, mv, acc, cu, pad, B, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status attn_thd_accumulate(attn_dtype dtype, int T, int H, int D, attn_tensor src, float *acc, int accumulate,
+                                const int32_t *cu_seqlens, const int32_t *cu_seqlens_padded, int B,
+                                attn_stream_t stream) {
+    return thd_rows("attn_thd_accumulate", dtype, T, H, D, src, acc, cu_seqlens, cu_seqlens_padded, B,
+                    accumulate ? 0 : 2, stream);
+}
+
+attn_status attn_thd_store(attn_dtype dtype, int T, int H, int D, const float *acc, attn_tensor dst,
+                           const int32_t *cu_seqlens, const int32_t *cu_seqlens_padded, int B,
+                           attn_stream_t stream) {
+    return thd_rows("attn_thd_store", dtype, T, H, D, dst, const_cast<float *>(acc), cu_seqlens, cu_seqlens_padded,
+                    B, 1, stream);
+}
+
 attn_status attn_profile_begin(int max_launches) {
     t_error.clear();
     if (max_launches < 1) return fail(ATTN_ERR_INVALID_ARG, "max_launches must be positive");

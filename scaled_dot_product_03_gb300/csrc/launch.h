@@ -61,6 +61,12 @@ struct MergeBwdArgs {
     float *dlse1, *dlse2;
 };
 cudaError_t launch_merge_bwd(int dtype, const MergeBwdArgs &a, cudaStream_t st);
+// THD row sums of the emulated context-parallel backward: mode 0 adds the
+// rows of v inside a sequence into acc, mode 2 copies them there, mode 1
+// writes acc into v (0 outside every sequence).  acc: [T, H, D] fp32
+// contiguous.
+cudaError_t launch_thd_rows(int dtype, int mode, int T, int H, int D, const MutView &v, float *acc, const int *cu,
+                            const int *pad, int B, cudaStream_t st);
 cudaError_t launch_partitioned_indices(const int *pad, int B, int world, int rank, int n_out, int *out,
                                        cudaStream_t st);
 

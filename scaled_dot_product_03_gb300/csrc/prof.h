@@ -21,6 +21,7 @@ enum ProfKind {
     kProfBwdDqConvert = 9,
     kProfMergeBwd = 10,
     kProfBwdDkvReduce = 11,
+    kProfThdRows = 12,
 };
 
 void prof_before(cudaStream_t st, int kind);

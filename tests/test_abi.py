@@ -186,6 +186,28 @@ def test_partitioned_indices_rejects_bad_args(lib):
     assert f(None, 0, 0, 2, 1, None, None) == _lib.ATTN_OK                 # empty: nothing
 
 
+def test_thd_row_sums_reject_bad_args(lib):
+    """attn_thd_accumulate / attn_thd_store validate before any launch."""
+    def tensor(ptr=4096, row=256, head=64):
+        t = _lib.AttnTensor()
+        t.ptr = ptr
+        t.stride[:] = (0, row, head, 1)
+        return t
+    cu, acc = 4096, 8192
+    for fn, call in (("accumulate", lambda dt, T, H, D, t, a, c, B: lib.attn_thd_accumulate(dt, T, H, D, t, a, 1, c, None, B, None)),
+                     ("store", lambda dt, T, H, D, t, a, c, B: lib.attn_thd_store(dt, T, H, D, a, t, c, None, B, None))):
+        assert call(9, 4, 2, 64, tensor(), acc, cu, 1) == _lib.ATTN_ERR_INVALID_ARG, fn      # dtype
+        assert call(1, 4, 2, 12, tensor(), acc, cu, 1) == _lib.ATTN_ERR_INVALID_ARG, fn      # D % 8
+        assert call(1, 4, 2, 264, tensor(), acc, cu, 1) == _lib.ATTN_ERR_INVALID_ARG, fn     # D > 256
+        assert call(1, -1, 2, 64, tensor(), acc, cu, 1) == _lib.ATTN_ERR_INVALID_ARG, fn     # T < 0
+        assert call(1, 4, 2, 64, tensor(), acc, None, 1) == _lib.ATTN_ERR_INVALID_ARG, fn    # cu_seqlens
+        assert call(1, 4, 2, 64, tensor(), acc, cu, 0) == _lib.ATTN_ERR_INVALID_ARG, fn      # B
+        assert call(1, 4, 2, 64, tensor(ptr=4098), acc, cu, 1) == _lib.ATTN_ERR_INVALID_ARG, fn  # alignment
+        assert call(1, 4, 2, 64, tensor(row=252), acc, cu, 1) == _lib.ATTN_ERR_INVALID_ARG, fn   # row stride
+        assert call(1, 4, 2, 64, tensor(), 8196, cu, 1) == _lib.ATTN_ERR_INVALID_ARG, fn     # acc alignment
+        assert call(1, 0, 2, 64, tensor(), acc, cu, 1) == _lib.ATTN_OK, fn                   # empty: no-op
+
+
 def test_header_is_c99_and_layout_matches_binding(tmp_path):
     """The header compiles as plain C99 with warnings as errors, and a C
     compiler lays attn_params and attn_tensor out exactly as the ctypes
