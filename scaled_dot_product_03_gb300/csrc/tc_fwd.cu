@@ -60,7 +60,7 @@ struct FwdCfg {
 };
 
 struct Bars {
-    uint64_t q_full;
+    uint64_t q_full[kMaxNQ];  // one per query tile: tile 0 starts before tile 1's Q lands
     uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
     uint64_t s_full[kMaxNQ], p_full[kMaxNQ], pv_done[kMaxNQ];
     uint32_t tmem_base;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
-        mbar_init(&bar.q_full, 1);
+        for (int i = 0; i < kMaxNQ; ++i) mbar_init(&bar.q_full[i], 1);
         for (int i = 0; i < KS; ++i) {
             mbar_init(&bar.k_full[i], 1);
             mbar_init(&bar.k_empty[i], 1);
@@ -179,11 +179,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     if (warp == kProdWarp) {
         // ------------------------------------------------------------ TMA
         if (lane == 0 && nb > 0) {
-            mbar_arrive_expect_tx(&bar.q_full, NQ * C::kTileBytes);
-            for (int i = 0; i < NQ; ++i)
+            // Q of tile 0, the first K block, then the other tiles' Q: tile 0's
+            // first S product needs only the first two
+            auto load_q = [&](int i) {
+                mbar_arrive_expect_tx(&bar.q_full[i], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(smem + C::kQOff + i * C::kTileBytes + c * BM * 128, &tm_q,
-                                &bar.q_full, c * 64, q_row + i * BM, h, qb);
+                    tma_load_4d(smem + C::kQOff + i * C::kTileBytes + c * BM * 128, &tm_q, &bar.q_full[i], c * 64,
+                                q_row + i * BM, h, qb);
+            };
+            load_q(0);
             for (int jb = 0; jb < nb; ++jb) {
                 const int st = jb % KS;
                 const uint32_t ph = (jb / KS) & 1;
@@ -192,6 +196,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_4d(smem + C::kKOff + st * C::kTileBytes + c * BN * 128, &tm_k,
                                 &bar.k_full[st], c * 64, kv_row + jb * BN, hk, qb);
+                if (jb == 0)
+                    for (int i = 1; i < NQ; ++i) load_q(i);
                 if (!mbar_wait(&bar.v_empty[st], ph ^ 1, wd, 0x11)) break;
                 mbar_arrive_expect_tx(&bar.v_full[st], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
@@ -238,12 +244,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 __syncwarp();
             };
             auto in_range = [&](int i, int jb) { return jb >= tr[i].blo && jb < tr[i].bhi; };
-            bool ok = wait(&bar.q_full, 0, 0x20) && wait(&bar.k_full[0], 0, 0x21);
+            bool ok = wait(&bar.k_full[0], 0, 0x21);
             if (ok) {
 #pragma unroll
-                for (int i = 0; i < NQ; ++i)
+                for (int i = 0; i < NQ; ++i) {
+                    if (!(ok = wait(&bar.q_full[i], 0, 0x20))) break;
                     if (in_range(i, 0)) issue_s(i, 0);
-                commit(&bar.k_empty[0]);
+                }
+                if (ok) commit(&bar.k_empty[0]);
             }
             for (int jb = 0; ok && jb < nb; ++jb) {
                 const int st = jb % KS;
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             // still have it in flight) in the load's 128B-swizzled layout and
             // write it with TMA stores, which drop rows past a dense tensor's
             // end.  A THD tile ending inside the tensor is written row by row.
-            if (nb > 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, wd, 0x32))) ok = false;
+            if (nb > 0 && !__all_sync(0xffffffffu, mbar_wait(&bar.q_full[i], 0, wd, 0x32))) ok = false;
             uint8_t *stage = smem + C::kQOff + i * C::kTileBytes;
             const uint32_t srow = smem_u32(stage) + r * 128;
 #pragma unroll
