@@ -138,7 +138,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (threadIdx.x == 0) {
+    // TMA coordinates: (d, row, head, batch); THD views have one "batch"
+    const int qb = g.thd ? 0 : b, q_row = s.q0 + m0;
+    const int kv_row = s.kv0 + jlo;
+    auto load_q = [&](int i) {
+        mbar_arrive_expect_tx(&bar.q_full[i], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(smem + C::kQOff + i * C::kTileBytes + c * BM * 128, &tm_q, &bar.q_full[i], c * 64,
+                        q_row + i * BM, h, qb);
+    };
+    auto load_k = [&](int jb) {
+        const int st = jb % KS;
+        mbar_arrive_expect_tx(&bar.k_full[st], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(smem + C::kKOff + st * C::kTileBytes + c * BN * 128, &tm_k, &bar.k_full[st], c * 64,
+                        kv_row + jb * BN, hk, qb);
+    };
+    if (warp == kProdWarp && lane == 0) {
+        // The loading lane sets up the barriers and issues tile 0's Q and the
+        // first K block at once, so those loads overlap the TMEM allocation
+        // and the block-wide sync (tile 0's first S product needs only them).
         for (int i = 0; i < kMaxNQ; ++i) mbar_init(&bar.q_full[i], 1);
         for (int i = 0; i < KS; ++i) {
             mbar_init(&bar.k_full[i], 1);
@@ -153,15 +172,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         bar.abort_flag = 0;
         fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        if (nb > 0) {
+            load_q(0);
+            load_k(0);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&bar.tmem_base, 512);
         tmem_relinquish();
-    }
-    if (warp == kProdWarp && lane == 0) {
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
     }
     tc_fence_before();
     __syncthreads();
@@ -172,32 +193,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t sQ = smem_u32(smem + C::kQOff);
     const uint32_t sK = smem_u32(smem + C::kKOff);
     const uint32_t sV = smem_u32(smem + C::kVOff);
-    // TMA coordinates: (d, row, head, batch); THD views have one "batch"
-    const int qb = g.thd ? 0 : b, q_row = s.q0 + m0;
-    const int kv_row = s.kv0 + jlo;
 
     if (warp == kProdWarp) {
         // ------------------------------------------------------------ TMA
+        // (tile 0's Q and K block 0 were issued before the sync; the other
+        // tiles' Q follow K block 0)
         if (lane == 0 && nb > 0) {
-            // Q of tile 0, the first K block, then the other tiles' Q: tile 0's
-            // first S product needs only the first two
-            auto load_q = [&](int i) {
-                mbar_arrive_expect_tx(&bar.q_full[i], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(smem + C::kQOff + i * C::kTileBytes + c * BM * 128, &tm_q, &bar.q_full[i], c * 64,
-                                q_row + i * BM, h, qb);
-            };
-            load_q(0);
             for (int jb = 0; jb < nb; ++jb) {
                 const int st = jb % KS;
                 const uint32_t ph = (jb / KS) & 1;
-                if (!mbar_wait(&bar.k_empty[st], ph ^ 1, wd, 0x10)) break;
-                mbar_arrive_expect_tx(&bar.k_full[st], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(smem + C::kKOff + st * C::kTileBytes + c * BN * 128, &tm_k,
-                                &bar.k_full[st], c * 64, kv_row + jb * BN, hk, qb);
-                if (jb == 0)
+                if (jb > 0) {
+                    if (!mbar_wait(&bar.k_empty[st], ph ^ 1, wd, 0x10)) break;
+                    load_k(jb);
+                } else {
                     for (int i = 1; i < NQ; ++i) load_q(i);
+                }
                 if (!mbar_wait(&bar.v_empty[st], ph ^ 1, wd, 0x11)) break;
                 mbar_arrive_expect_tx(&bar.v_full[st], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
