@@ -137,43 +137,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_it = nqb * nh;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar.kv_full, 1);
-        for (int i = 0; i < QS; ++i) {
-            mbar_init(&bar.q_full[i], 32);
-            mbar_init(&bar.q_empty[i], 1);
-        }
-        mbar_init(&bar.k_tmem, kCompute);
-        mbar_init(&bar.s_full, 1);
-        mbar_init(&bar.p_full, kCompute);
-        mbar_init(&bar.dp_full, 1);
-        mbar_init(&bar.ds_full, kCompute);
-        mbar_init(&bar.dq_full, 1);
-        mbar_init(&bar.dq_free, kDrain);
-        mbar_init(&bar.acc_done, 1);
-        bar.abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(&bar.tmem_base, 512);
-        tmem_relinquish();
-    }
-    if (warp == kProdWarp && lane == 0) {
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-        prefetch_tmap(&tm_do);
-        prefetch_tmap(&tm_acc);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bar.tmem_base;
-    const Watchdog wd{a.watchdog_ns, a.err, &bar.abort_flag};
     const int cb = g.thd ? 0 : b;  // TMA batch coordinate
-
+    // Block t's LSE (log2 units) and delta into stage t % QS, then its Q and
+    // dO loads (the whole producer warp; lane 0 arms the stage).  With a
+    // watchdog, the stage's previous block must have been consumed first;
+    // the statistics are fetched before that wait.
+    auto stage_block = [&](int t, const Watchdog *w) {
+        const int st = t % QS;
+        const uint32_t ph = (t / QS) & 1;
+        const int h = h0 + t / nqb;
+        const int i0 = ilo + (t % nqb) * BQ;
+        float lv[2], dv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + lane + 32 * u;
+            lv[u] = dv[u] = 0.f;
+            if (i < s.Lq) {
+                const int64_t li = lse_index(g, s, b, h, i);
+                lv[u] = a.lse[li] * kLog2e;
+                dv[u] = a.delta[li];
+            }
+        }
+        if (w && !__all_sync(0xffffffffu, mbar_wait(&bar.q_empty[st], ph ^ 1, *w, 0xc0))) return false;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            s_lse[st * BQ + lane + 32 * u] = lv[u];
+            s_delta[st * BQ + lane + 32 * u] = dv[u];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar.q_full[st], 2 * kQTile);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_4d(smem + kQOff + st * kQTile + c * BQ * 128, &tm_q, &bar.q_full[st], c * 64, s.q0 + i0, h,
+                            cb);
+                tma_load_4d(smem + kDOOff + st * kQTile + c * BQ * 128, &tm_do, &bar.q_full[st], c * 64, s.q0 + i0,
+                            h, cb);
+            }
+        } else {
+            mbar_arrive(&bar.q_full[st]);
+        }
+        return true;
+    };
     if (warp == kProdWarp) {
-        // ------------------------------------------------------------ loads
+        // The producer warp sets up the barriers and issues K, V and the first
+        // block's loads at once, so they overlap the TMEM allocation and the
+        // block-wide sync (stage 0 is free).
+        if (lane == 0) {
+            mbar_init(&bar.kv_full, 1);
+            for (int i = 0; i < QS; ++i) {
+                mbar_init(&bar.q_full[i], 32);
+                mbar_init(&bar.q_empty[i], 1);
+            }
+            mbar_init(&bar.k_tmem, kCompute);
+            mbar_init(&bar.s_full, 1);
+            mbar_init(&bar.p_full, kCompute);
+            mbar_init(&bar.dp_full, 1);
+            mbar_init(&bar.ds_full, kCompute);
+            mbar_init(&bar.dq_full, 1);
+            mbar_init(&bar.dq_free, kDrain);
+            mbar_init(&bar.acc_done, 1);
+            bar.abort_flag = 0;
+            fence_mbar_init();
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            prefetch_tmap(&tm_acc);
+        }
+        __syncwarp();
         if (n_it > 0) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bar.kv_full, 2 * kKVTile);
@@ -182,44 +213,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(smem + kVOff + c * BK * 128, &tm_v, &bar.kv_full, c * 64, s.kv0 + n0, hk, cb);
                 }
             }
-            for (int t = 0; t < n_it; ++t) {
-                const int st = t % QS;
-                const uint32_t ph = (t / QS) & 1;
-                const int h = h0 + t / nqb;
-                const int i0 = ilo + (t % nqb) * BQ;
-                // LSE (log2 units) and delta of the block's rows, fetched while
-                // the stage is still in use
-                float lv[2], dv[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int i = i0 + lane + 32 * u;
-                    lv[u] = dv[u] = 0.f;
-                    if (i < s.Lq) {
-                        const int64_t li = lse_index(g, s, b, h, i);
-                        lv[u] = a.lse[li] * kLog2e;
-                        dv[u] = a.delta[li];
-                    }
-                }
-                if (!__all_sync(0xffffffffu, mbar_wait(&bar.q_empty[st], ph ^ 1, wd, 0xc0))) break;
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    s_lse[st * BQ + lane + 32 * u] = lv[u];
-                    s_delta[st * BQ + lane + 32 * u] = dv[u];
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bar.q_full[st], 2 * kQTile);
-                    for (int c = 0; c < D / 64; ++c) {
-                        tma_load_4d(smem + kQOff + st * kQTile + c * BQ * 128, &tm_q, &bar.q_full[st], c * 64,
-                                    s.q0 + i0, h, cb);
-                        tma_load_4d(smem + kDOOff + st * kQTile + c * BQ * 128, &tm_do, &bar.q_full[st], c * 64,
-                                    s.q0 + i0, h, cb);
-                    }
-                } else {
-                    mbar_arrive(&bar.q_full[st]);
-                }
-            }
+            stage_block(0, nullptr);
         }
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bar.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+    const Watchdog wd{a.watchdog_ns, a.err, &bar.abort_flag};
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------------------ loads
+        for (int t = 1; t < n_it; ++t)
+            if (!stage_block(t, &wd)) break;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA
         // Per block t: dV_t (once P_t is written), S^T_{t+1} (its TMEM held
