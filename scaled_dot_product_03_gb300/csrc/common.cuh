@@ -168,6 +168,14 @@ struct FastDiv {
     }
 };
 
+// Programmatic dependent launch.  griddep_wait: wait until the grids this
+// one depends on have completed and their writes are visible (returns at
+// once for a grid launched without the dependency).  griddep_launch: let the
+// grid that depends on this one begin launching once every CTA of this grid
+// has issued it (or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }

@@ -1,6 +1,8 @@
 // launch.h -- host-side launchers of the library's kernels (internal).
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace gbattn {
@@ -44,6 +46,26 @@ struct MergeArgs {
 
 // Streaming multiprocessors of the current device (queried once per device).
 cudaError_t device_sm_count(int *out);
+
+// Launches kern on st with programmatic stream serialization: the grid may
+// begin while the previous kernel on the stream is finishing (once that
+// kernel's CTAs have issued griddep_launch), so kern must griddep_wait
+// before it reads anything the previous kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // dtype: 0 = fp16, 1 = bf16, 2 = fp32 (same values as attn_dtype).
 cudaError_t launch_simt_fwd(int dtype, const FwdArgs &a, int max_lq, cudaStream_t st);

@@ -182,6 +182,10 @@ template <typename T, int VEC>
 __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
     struct alignas(sizeof(T) * VEC) Vt { T v[VEC]; };
     const Geometry &g = a.g;
+    // (launched as a dependent of the previous kernel: wait for it, then let
+    // the backward's next kernel begin launching)
+    griddep_wait();
+    griddep_launch();
     const int D = g.D;
     const int chunks = D / VEC;
     const int tpr = lanes_per_row(chunks);
@@ -245,6 +249,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess16_kernel(BwdArgs a, int ro
     constexpr int LPR = NV <= 4 ? 4 : NV <= 8 ? 8 : 16;   // lanes per row
     constexpr int RPW = 32 / LPR;                         // rows per warp and group
     const Geometry &g = a.g;
+    griddep_wait();
+    griddep_launch();
     const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
     const unsigned pairs = (unsigned)rows * (unsigned)g.Hq;
     const unsigned nwarps = gridDim.x * (blockDim.x / 32);
@@ -605,7 +611,9 @@ void preprocess_typed(const BwdArgs &a, int rows, cudaStream_t st) {
     const int tpr = lanes_per_row(a.g.D / VEC);
     const int64_t warps = ((int64_t)rows * a.g.Hq + (32 / tpr) - 1) / (32 / tpr);
     int64_t blocks = (warps + 7) / 8;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    int sms = 0;
+    if (device_sm_count(&sms) != cudaSuccess) sms = 1;
+    if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;  // grid-stride beyond 16 blocks per SM
     if (blocks < 1) blocks = 1;
     prof_before(st, kProfBwdPreprocess);
     bwd_preprocess_kernel<T, VEC><<<(unsigned)blocks, 256, 0, st>>>(a, rows);
@@ -636,10 +644,10 @@ cudaError_t preprocess16_typed(const BwdArgs &a, int rows, cudaStream_t st) {
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks < 1) blocks = 1;
     prof_before(st, kProfBwdPreprocess);
-    bwd_preprocess16_kernel<T, D, U><<<(unsigned)blocks, 256, 0, st>>>(a, rows, FastDiv(a.g.Hq),
-                                                                       FastDiv(a.g.Sq > 0 ? a.g.Sq : 1));
+    cudaError_t le = launch_pdl(bwd_preprocess16_kernel<T, D, U>, dim3((unsigned)blocks), dim3(256), 0, st, a, rows,
+                                FastDiv(a.g.Hq), FastDiv(a.g.Sq > 0 ? a.g.Sq : 1));
     prof_after(st);
-    return cudaGetLastError();
+    return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 template <typename T>

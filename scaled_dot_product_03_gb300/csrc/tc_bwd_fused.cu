@@ -108,6 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Bars &bar = *reinterpret_cast<Bars *>(smem + kBarOff);
+    // Launched as a dependent of the preprocess: everything up to the first
+    // read of its output (delta, the cleared dQ accumulator) overlaps its
+    // tail; the dQ conversion may begin launching at once.
+    griddep_launch();
     float *s_lse = reinterpret_cast<float *>(smem + kStatOff);  // log2 units
     float *s_delta = s_lse + QS * BQ;
     const Geometry &g = a.g;
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(smem + kVOff + c * BK * 128, &tm_v, &bar.kv_full, c * 64, s.kv0 + n0, hk, cb);
                 }
             }
+            griddep_wait();  // delta comes from the preprocess
             stage_block(0, nullptr);
         }
     }
@@ -505,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kDrainWarp0) {
         // ----------------------------------- dQ^T drain (thread = head dim)
+        griddep_wait();  // the accumulator is cleared by the preprocess
         const int qd = warp % 4;  // TMEM lane quarter = head dims [32 qd, 32 qd + 32)
         const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
         const uint32_t box = smem_u32(smem + kStgOff) + qd * kBox;
@@ -624,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <typename T, int DD, int U>
 __global__ void __launch_bounds__(256)
     dq_convert_kernel(MutView dq, const float *__restrict__ acc, Geometry g, FastDiv fRows, FastDiv fHq) {
+    griddep_wait();  // the accumulator is complete once the single pass has finished
     constexpr int LPR = DD / 8;
     constexpr int RPW = 32 / LPR;
     const unsigned rows = g.thd ? (unsigned)g.Hq * (unsigned)g.Tq : (unsigned)g.B * (unsigned)g.Hq * (unsigned)g.Sq;
@@ -678,6 +685,7 @@ __global__ void __launch_bounds__(256)
 template <typename T, int DD>
 __global__ void __launch_bounds__(256)
     dkv_reduce_kernel(MutView dk, MutView dv, const float *__restrict__ part, int nsplit, Geometry g) {
+    griddep_wait();  // the partials are complete once the single pass has finished
     constexpr int LPR = DD / 8;
     constexpr int RPW = 32 / LPR;
     const unsigned nrows = g.thd ? (unsigned)g.Skv : (unsigned)g.B * (unsigned)g.Skv;
@@ -765,9 +773,10 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
         const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B * a.nsplit;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdFused);
-        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, tgk, tgv, a, n_ktiles);
+        e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, tq, tk, tv, tdo, tacc, tgk, tgv, a,
+                       n_ktiles);
         prof_after(st);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
         if (a.dkv_part && (e = launch_dkv_reduce(dt, a, st)) != cudaSuccess) return e;
     } else if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) {
         return e;
@@ -788,9 +797,10 @@ cudaError_t dkv_reduce_typed(const BwdArgs &a, cudaStream_t st) {
     int64_t blocks = (warps + 7) / 8;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     prof_before(st, kProfBwdDkvReduce);
-    dkv_reduce_kernel<T, DD><<<(unsigned)blocks, 256, 0, st>>>(a.dk, a.dv, a.dkv_part, a.nsplit, g);
+    cudaError_t le = launch_pdl(dkv_reduce_kernel<T, DD>, dim3((unsigned)blocks), dim3(256), 0, st, a.dk, a.dv,
+                                a.dkv_part, a.nsplit, g);
     prof_after(st);
-    return cudaGetLastError();
+    return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 template <typename T, int DD>
@@ -809,10 +819,10 @@ cudaError_t dq_convert_typed(const BwdArgs &a, cudaStream_t st) {
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     prof_before(st, kProfBwdDqConvert);
     const int per_head = g.thd ? g.Tq : g.Sq;
-    dq_convert_kernel<T, DD, U><<<(unsigned)blocks, 256, 0, st>>>(a.dq, a.dq_acc, g, FastDiv(per_head > 0 ? per_head : 1),
-                                                                  FastDiv(g.Hq));
+    cudaError_t le = launch_pdl(dq_convert_kernel<T, DD, U>, dim3((unsigned)blocks), dim3(256), 0, st, a.dq, a.dq_acc, g,
+                                FastDiv(per_head > 0 ? per_head : 1), FastDiv(g.Hq));
     prof_after(st);
-    return cudaGetLastError();
+    return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 }  // namespace

@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Bars &bar = *reinterpret_cast<Bars *>(smem + kBarOff);
+    // Launched as a dependent of the preprocess: everything up to the first
+    // read of its output (delta, the cleared dQ accumulator) overlaps its
+    // tail; the dQ conversion may begin launching at once.
+    griddep_launch();
     float *s_lse = reinterpret_cast<float *>(smem + kStatOff);  // log2 units
     float *s_delta = s_lse + QS * BQ;
     const Geometry &g = a.g;
@@ -165,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(smem + kKOff, &tm_k, &bar.kv_full, 0, s.kv0 + n0, hk, cb);
                 tma_load_4d(smem + kVOff, &tm_v, &bar.kv_full, 0, s.kv0 + n0, hk, cb);
             }
+            griddep_wait();  // delta comes from the preprocess
             for (int t = 0; t < n_it; ++t) {
                 const int st = t % QS;
                 const uint32_t ph = (t / QS) & 1;
@@ -442,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kDrainWarp0) {
         // ------------------------------------- dQ drain (thread = query row)
+        griddep_wait();  // the accumulator is cleared by the preprocess
         const int qd = warp % 4;  // TMEM lane quarter = query rows [32 qd, 32 qd + 32)
         const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
         const uint32_t box0 = smem_u32(smem + kStgOff) + qd * 2 * kBox;  // head dims 0-31, then 32-63
@@ -529,9 +535,10 @@ cudaError_t launch_typed(const BwdArgs &a, int max_lkv, int q_rows, cudaStream_t
         const int64_t grid = (int64_t)n_ktiles * g.Hkv * g.B * a.nsplit;
         if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
         prof_before(st, kProfBwdFused);
-        kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, tdo, tacc, tgk, tgv, a, n_ktiles);
+        e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, tq, tk, tv, tdo, tacc, tgk, tgv, a,
+                       n_ktiles);
         prof_after(st);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
         if (a.dkv_part && (e = launch_dkv_reduce(dt, a, st)) != cudaSuccess) return e;
     } else if ((e = launch_bwd_preprocess(dt, a, q_rows, st)) != cudaSuccess) {
         return e;
