@@ -220,7 +220,7 @@ int64_t kv_rows(const attn_params *p) {
 }
 
 struct WsLayout {
-    size_t delta_off, acc_off, part_off, total;
+    size_t delta_off, acc_off, part_off, ctr_off, total;
     bool fused;
     int nsplit;
 };
@@ -228,7 +228,7 @@ struct WsLayout {
 // Workspace: the fp32 row terms delta_i = <dO_i, O_i>, laid out like LSE,
 // then (single-pass backward only) the fp32 dq accumulator, D floats per
 // LSE entry, then (split query heads only) the fp32 partial dK and dV of
-// every split.
+// every split, then (single pass) the work counter of its persistent CTAs.
 WsLayout ws_layout(const attn_params *p) {
     WsLayout w;
     const size_t rows = (size_t)q_rows(p) * p->Hq;
@@ -242,6 +242,8 @@ WsLayout ws_layout(const attn_params *p) {
     w.total = w.part_off;
     if (w.nsplit > 1)
         w.total += round_up(sizeof(float) * (size_t)w.nsplit * 2 * kv_rows(p) * p->Hkv * dc, 256);
+    w.ctr_off = w.total;
+    if (w.fused) w.total += 256;
     return w;
 }
 
@@ -413,6 +415,7 @@ attn_status bwd_impl(const attn_params *p, attn_tensor q, attn_tensor k, attn_te
     a.nsplit = w.nsplit;
     a.acc_d = tc_dim(p->D);
     a.dkv_part = w.nsplit > 1 ? (float *)((char *)workspace + w.part_off) : nullptr;
+    a.work_ctr = w.fused ? (unsigned *)((char *)workspace + w.ctr_off) : nullptr;
     a.watchdog_ns = watchdog_ns();
     if ((st = device_error_word(&a.err))) return st;
     const cudaStream_t s = (cudaStream_t)stream;

@@ -32,6 +32,8 @@ struct BwdArgs {
     int nsplit = 1;       // query-head splits per key tile (1: none)
     int acc_d = 0;        // floats per row of dq_acc and of the partials (the
                           // tensor-core head dim, tc_dim(D))
+    unsigned *work_ctr = nullptr;  // persistent single pass: items taken after
+                          // each CTA's first, zeroed by the preprocess kernel
     unsigned *err;
     uint64_t watchdog_ns;
 };

@@ -177,7 +177,8 @@ __host__ __device__ inline int lanes_per_row(int chunks) {
 // no LSE gradient is given).  A group of up to 32
 // lanes (power of two) covers one (row, head), each lane VEC elements at a
 // time.  Also clears the fp32 dq accumulator (laid out like LSE, D floats per
-// row) when the backward uses one.
+// row) and the work counter of the persistent single pass when the backward
+// uses them.
 template <typename T, int VEC>
 __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
     struct alignas(sizeof(T) * VEC) Vt { T v[VEC]; };
@@ -186,6 +187,7 @@ __global__ void bwd_preprocess_kernel(BwdArgs a, int rows) {
     // the backward's next kernel begin launching)
     griddep_wait();
     griddep_launch();
+    if (a.work_ctr && blockIdx.x == 0 && threadIdx.x == 0) *a.work_ctr = 0u;
     const int D = g.D;
     const int chunks = D / VEC;
     const int tpr = lanes_per_row(chunks);
@@ -251,6 +253,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess16_kernel(BwdArgs a, int ro
     const Geometry &g = a.g;
     griddep_wait();
     griddep_launch();
+    if (a.work_ctr && blockIdx.x == 0 && threadIdx.x == 0) *a.work_ctr = 0u;
     const int lane = threadIdx.x & 31, sub = lane / LPR, c = lane % LPR;
     const unsigned pairs = (unsigned)rows * (unsigned)g.Hq;
     const unsigned nwarps = gridDim.x * (blockDim.x / 32);

@@ -31,6 +31,18 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Element-wise product of two packed pairs, rounded to nearest.
+template <typename T> __device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ uint32_t mul2<__nv_bfloat16>(uint32_t a, uint32_t b) {
+    const __nv_bfloat162 r =
+        __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&a), *reinterpret_cast<const __nv_bfloat162 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+template <> __device__ __forceinline__ uint32_t mul2<__half>(uint32_t a, uint32_t b) {
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -63,6 +75,41 @@ __device__ __forceinline__ void store_f32_row32(float *dst, const uint32_t (&v)[
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
     for (int e = 0; e < 8; ++e) d4[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+}
+
+// One work item of a persistent single-pass backward: the BK keys of key
+// tile kt of a (batch, key/value head, query-head split), decoded from its
+// index w in the banded, heaviest-first order.
+struct BwdItem {
+    SeqInfo s;
+    int b, hk, sp, kt;
+    int n0, nkeys;   // first key, keys in the tile (<= 0: the tile is past the sequence)
+    int h0, nh;      // query heads [h0, h0 + nh)
+    int ilo, nqb;    // first query row seeing the tile, query blocks per head
+    int n_it;        // blocks: nqb * nh
+};
+
+__device__ __forceinline__ BwdItem bwd_item(int w, const Geometry &g, int nsplit, int n_ktiles, int bk, int bq,
+                                            int band) {
+    BwdItem it;
+    int bhs;
+    banded_order(w, n_ktiles, g.Hkv * g.B * nsplit, bhs, it.kt, band);
+    it.sp = bhs % nsplit;
+    const int bh = bhs / nsplit;
+    it.hk = bh % g.Hkv;
+    it.b = bh / g.Hkv;
+    it.s = seq_info(g, it.b);
+    it.n0 = it.kt * bk;
+    it.nkeys = min(bk, it.s.Lkv - it.n0);
+    const int gs = (g.G + nsplit - 1) / nsplit;
+    it.h0 = it.hk * g.G + it.sp * gs;
+    it.nh = max(0, min(gs, g.G - it.sp * gs));
+    int ihi = 0;
+    it.ilo = 0;
+    if (it.nkeys > 0) query_range(it.n0, it.n0 + it.nkeys, it.s.Lq, g.wl, g.wr, it.ilo, ihi);
+    it.nqb = (ihi - it.ilo + bq - 1) / bq;
+    it.n_it = it.nkeys > 0 ? it.nqb * it.nh : 0;
+    return it;
 }
 
 }  // namespace tcu

@@ -184,6 +184,41 @@ def test_varlen_thd_gqa_fwd_bwd_sampled(det):
     check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
 
 
+@pytest.mark.parametrize("window,dtype", [((-1, 0), torch.bfloat16), ((-1, -1), torch.float16),
+                                          ((63, 0), torch.bfloat16)])
+def test_d64_many_short_items_sampled(window, dtype):
+    """Head dim 64 at S=256 over 32 sequences and 16 heads: 1024 key tiles of
+    one or two query blocks each, several per CTA of the persistent single
+    pass (the next tile's loads and first products overlap the current
+    one's last), causal, full and a narrow band."""
+    prob = inputs.dense(32, 256, 16, 64, dtype=dtype, window=window, seed=11, dout_seed=12)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    rows = sample_rows(prob, 16, seed=5)
+    check_fwd(prob, o, lse, row_sel=rows)
+    keys = sample_keys(prob, [(0, 0), (13, 7), (31, 15)], 32, seed=6)
+    check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
+
+
+def test_d64_thd_mixed_lengths_sampled():
+    """Packed THD at head dim 64, 40 sequences of 1 to 700 tokens (GQA 4:1):
+    the key tiles past a short sequence's end are items without rows, those
+    that no query sees have zero gradients, and the others vary from one to
+    six blocks per query head."""
+    prob = inputs.varlen(nseq=40, min_len=1, max_len=700, Hq=8, Hkv=2, D=64, len_seed=7, seed=8,
+                         dout_seed=9)
+    d = _dev(prob)
+    o, lse = run_fwd(d)
+    dq, dk, dv = run_bwd(d, o, lse)
+    _sync_ok()
+    rows = sample_rows(prob, 48, seed=3)
+    check_fwd(prob, o, lse, row_sel=rows)
+    keys = sample_keys(prob, [(0, 0), (17, 1), (39, 1)], 24, seed=4)
+    check_bwd(prob, dq, dk, dv, row_sel=rows, key_sel=keys)
+
+
 # ---------------------------------------------------------------- edge cases
 
 # (dtype, D, deterministic): the 16-bit backward at D=64 and 128 has a
