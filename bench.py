@@ -30,7 +30,7 @@ WORKLOAD = dict(B=4, S=4096, H=16, D=128, window=(-1, 0))
 # DRAM bytes (read + write) per launch of the dominant kernel on this workload,
 # from a one-kernel ncu capture of this command (dram__bytes metrics; see
 # profiles/); None when the kernel changed after the capture.
-TRAFFIC = {"bwd_fused": 626099456}
+TRAFFIC = {"bwd_fused": 626503168}
 METRIC = "attention TFLOP/s fwd+bwd (bf16 causal) and % of GB300 dense BF16 tensor peak"
 
 
