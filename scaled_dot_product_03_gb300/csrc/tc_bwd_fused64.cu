@@ -458,34 +458,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // live across the wait for dP^T
                 uint32_t pp[32];
                 {
-                    float p[64];
+                    // query columns [clo, chi) of this half see the key
+                    int clo = 0, chi = 64;
+                    if (!full) {
+                        chi = min(64, s.Lq - i0);
+                        if (g.wr >= 0) clo = max(clo, key - g.wr - i0);
+                        if (g.wl >= 0) chi = min(chi, key + g.wl + 1 - i0);
+                        if (key >= s.Lkv) chi = clo;
+                    }
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
+                        // 32 columns at a time: exp2, mask, pack
                         uint32_t sr[32];
                         tmem_ld32(tS + 32 * h2, sr);
                         // 16-byte broadcast reads of the LSE (shared memory
                         // bandwidth is shared with the MMA operand reads)
                         const float4 *l4 = reinterpret_cast<const float4 *>(lse2 + 32 * h2);
+                        float p[32];
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const float4 l = l4[q];
-                            p[32 * h2 + 4 * q] = ex2(fmaf(__uint_as_float(sr[4 * q]), c2, -l.x));
-                            p[32 * h2 + 4 * q + 1] = ex2(fmaf(__uint_as_float(sr[4 * q + 1]), c2, -l.y));
-                            p[32 * h2 + 4 * q + 2] = ex2(fmaf(__uint_as_float(sr[4 * q + 2]), c2, -l.z));
-                            p[32 * h2 + 4 * q + 3] = ex2(fmaf(__uint_as_float(sr[4 * q + 3]), c2, -l.w));
+                            p[4 * q] = ex2(fmaf(__uint_as_float(sr[4 * q]), c2, -l.x));
+                            p[4 * q + 1] = ex2(fmaf(__uint_as_float(sr[4 * q + 1]), c2, -l.y));
+                            p[4 * q + 2] = ex2(fmaf(__uint_as_float(sr[4 * q + 2]), c2, -l.z));
+                            p[4 * q + 3] = ex2(fmaf(__uint_as_float(sr[4 * q + 3]), c2, -l.w));
                         }
-                    }
-                    if (!full) {
-                        int clo = 0, chi = min(64, s.Lq - i0);
-                        if (g.wr >= 0) clo = max(clo, key - g.wr - i0);
-                        if (g.wl >= 0) chi = min(chi, key + g.wl + 1 - i0);
-                        if (key >= s.Lkv) chi = clo;
+                        if (!full) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c < clo || c >= chi) p[c] = 0.f;
-                    }
+                            for (int c = 0; c < 32; ++c)
+                                if (32 * h2 + c < clo || 32 * h2 + c >= chi) p[c] = 0.f;
+                        }
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) pp[c] = pack2<T>(p[2 * c], p[2 * c + 1]);
+                        for (int c = 0; c < 16; ++c) pp[16 * h2 + c] = pack2<T>(p[2 * c], p[2 * c + 1]);
+                    }
                 }
                 tmem_st32(tS, pp);
                 tmem_wait_st();
