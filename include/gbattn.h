@@ -159,8 +159,9 @@ GBATTN_API attn_status attn_fwd(const attn_params *p, attn_tensor q, attn_tensor
  * bf16) the query heads of each group are split over several CTAs, and the
  * workspace also holds every split's fp32 partial dK and dV (2 D' floats per
  * key row and key/value head per split), summed in split order, so dK and dV
- * stay reproducible.  The single pass also keeps a 256-byte block for the
- * work counter of its persistent CTAs (cleared on the stream by each call).
+ * stay reproducible.  Every single-pass workspace also keeps a 256-byte
+ * block for the work counter that the persistent CTAs of the D' = 64 single
+ * pass take their key tiles from (cleared on the stream by each call).
  * Returns 0 for invalid parameters.
  */
 GBATTN_API size_t attn_bwd_workspace_size(const attn_params *p);
