@@ -867,6 +867,9 @@ def _profile_cases():
         "causal_bf16_b2_s4096_h16_d128_mqa": ("query-head split and the dK/dV reduce (one KV head)",
                                               lambda: fwd_bwd(inputs.dense(2, 4096, 16, 128, Hkv=1, seed=3,
                                                                            dout_seed=4))),
+        "causal_fp16_b1_s2048_h16_hkv1_d64_page1": ("the page-1 multi-query workload: single pass at D=64 "
+                                                    "with 16 query-head splits, dK/dV reduce",
+                                                    lambda: fwd_bwd(inputs.page1(scale=0.1, dout_seed=5))),
         "causal_bf16_b1_s8192_h8_d256": ("tc_fwd<bf16,256> (forward only)",
                                          lambda: fwd_bwd(inputs.dense(1, 8192, 8, 256, seed=3, dout_seed=None))),
         "fp32_causal_b4_s2048_h16_d64": ("FFMA forward, dq and dk/dv kernels",
